@@ -1,0 +1,66 @@
+"""Plausible mistakes planted in copies of the oracle (on the CPU) must each be
+caught by at least one pin.  This shows the pins constrain every part of the
+oracle: ordering, offsets, filtering, the row copy, the reduction and the
+rounding.  Each mutant runs in a child process, because some planted mistakes
+index out of bounds; a crash of the child also counts as caught."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "moe_oracle.c")
+TESTS = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(TESTS)
+
+MUTANTS = {
+    "unstable_order": ("for (int64_t r = 0; r < R; ++r) {\n        if (key[r] < 0) {",
+                       "for (int64_t r = R - 1; r >= 0; --r) {\n        if (key[r] < 0) {"),
+    "inclusive_offsets": ("cursor[e] = offsets[e];", "cursor[e] = offsets[e + 1] - (count[e] > 0);"),
+    "row_from_p_not_r": ("(const char *)hidden + t * row_bytes",
+                         "(const char *)hidden + (p / K) * row_bytes"),
+    "map_minus_one_flagged": ("if (e == -1)\n        return -1;", ""),
+    "tail_not_filled": ("permuted_idx[p] = -1;\n\n    free", "(void)p;\n\n    free"),
+    "id_range_off_by_one": ("g >= (int64_t)E", "g > (int64_t)E"),
+    "drop_last_k": ("for (int32_t k = 0; k < K; ++k) {\n                int32_t p = inv",
+                    "for (int32_t k = 0; k < K - 1; ++k) {\n                int32_t p = inv"),
+    "weight_transposed": ("float prod = w[t * K + k] * x;", "float prod = w[k * T + t] * x;"),
+    "truncate_not_round": ("kept += 1u;", "kept += 0u;"),
+    "ties_away_from_zero": ("(dropped == 0x8000u && (kept & 1u))", "(dropped == 0x8000u)"),
+    "subtract_term": ("acc = acc + prod;", "acc = acc - prod;"),
+    "scale_row_wrong_token": ("scales + t * scale_cols", "scales + (t / 2) * scale_cols"),
+}
+
+CHILD = r"""
+import sys
+sys.path[:0] = [{root!r}, {tests!r}]
+import oracle, pins
+orc = oracle.OracleLib({so!r})
+caught = []
+for pin in pins.ALL_PINS:
+    try:
+        pin(orc)
+    except AssertionError:
+        caught.append(pin.__name__)
+print("CAUGHT:" + ",".join(caught))
+"""
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    old, new = MUTANTS[name]
+    with open(SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique/found"
+    path = tmp_path / f"{name}.c"
+    path.write_text(src.replace(old, new))
+    so = oracle.compile_source(str(path), str(tmp_path / f"lib{name}.so"))
+    code = CHILD.format(root=ROOT, tests=TESTS, so=so)
+    proc = subprocess.run([sys.executable, "-c", code], capture_output=True,
+                          text=True, timeout=300)
+    if proc.returncode != 0:
+        return  # the planted mistake crashed the child: caught
+    line = [ln for ln in proc.stdout.splitlines() if ln.startswith("CAUGHT:")][-1]
+    assert line != "CAUGHT:", f"no pin caught mutant {name}"
