@@ -1,0 +1,520 @@
+"""Benchmark of the MoE token permute -> unpermute path on GB300.
+
+One step = moe_permute (routing metadata + row gather) followed by
+moe_unpermute (weighted top-k reduce) over one batch of a Mixtral-8x7B-shaped
+MoE layer (T=16384 tokens, H=4096, E=8, top-2, bf16), through the C ABI.
+The metric is HBM throughput: algorithmic bytes the step must move divided by
+its device time, in GB/s, with the fraction of the measured HBM peak.  The
+per-op numbers, the token-count sweep over every workload shape and the T=1
+latencies come in the same JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--no-sweep] [--no-cpu-baseline]
+
+Multi-GPU (torchrun): every rank runs the same step on its own batch (the
+path has no exchange step; weak scaling); timing is max over ranks.
+--impl reference: the CPU oracle, timed on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from moe_token_permute_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "permute/unpermute HBM GB/s (% of GB300 peak) and µs/call vs token count"
+HEADLINE = ("mixtral", 16384)
+FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "moe_token_permute_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+
+
+# ------------------------------------------------------------ byte models ---
+def routing_counts(ids: torch.Tensor, emap, E: int, K: int):
+    """(T_v, N_v): tokens with >= 1 kept row, kept rows (host-side accounting)."""
+    g = ids.long()
+    ok = (g >= 0) & (g < E)
+    if emap is not None:
+        loc = torch.where(ok, emap.long()[g.clamp(0, E - 1)], torch.full_like(g, -1))
+        ok = loc >= 0
+    return int(ok.any(dim=1).sum()), int(ok.sum())
+
+
+def permute_bytes(T, H, K, E_L, elem, scale_cols, Tv, Nv):
+    """ids + source rows read once + K-fold row writes + both index maps + offsets."""
+    rb = H * elem + scale_cols * 4
+    return T * K * 4 + Tv * rb + Nv * rb + 2 * T * K * 4 + (E_L + 1) * 8
+
+
+def gather_kernel_bytes(T, H, K, elem, scale_cols, Tv, Nv):
+    rb = H * elem + scale_cols * 4
+    return T * K * 4 + Tv * rb + Nv * rb
+
+
+def unpermute_bytes(T, H, K, Nv):
+    """inv + weights + kept expert rows read + output written."""
+    return 2 * T * K * 4 + Nv * H * 2 + T * H * 2
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    """SM clock / throttle-reason samples via NVML (read-only queries)."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int, period_s: float = 0.002):
+        self.ok = False
+        self.samples = []
+        self.period = period_s
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            props = torch.cuda.get_device_properties(device_index)
+            bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                return
+            self.nv, self.h = nv, h
+            mx = ctypes.c_uint()
+            nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            self.max_mhz = int(mx.value)
+            self._reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.ok = True
+        except (OSError, AttributeError, RuntimeError):
+            self.ok = False
+
+    def _sample(self):
+        c = ctypes.c_uint()
+        r = ctypes.c_ulonglong()
+        self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(c))
+        self._reasons(self.h, ctypes.byref(r))
+        self.samples.append((int(c.value), int(r.value)))
+
+    def _loop(self):
+        while not self._stop.is_set():
+            self._sample()
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = threading.Event()
+            self._sample()
+            self._t = threading.Thread(target=self._loop, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+            self._sample()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return None
+        mhz = [s[0] for s in self.samples]
+        bits = 0
+        for _, r in self.samples:
+            bits |= r
+        reasons = sorted(n for b, n in self.REASONS.items() if bits & b)
+        return {"sm_mhz": float(statistics.median(mhz)), "sm_max_mhz": float(self.max_mhz),
+                "reasons": reasons, "samples": len(mhz), "source": "nvml"}
+
+
+# ---------------------------------------------------------------- helpers ---
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    for r in rec.get("kernels", []):
+        if r.get("kernel") == kernel and r.get("workload") == workload and \
+                r.get("source_sha") == kernel_source_sha():
+            return r.get("dram_bytes_per_launch")
+    return None
+
+
+class Setup:
+    """Device buffers for one (workload, T): inputs, outputs, workspace."""
+
+    def __init__(self, name, T, seed, dev):
+        import moe_token_permute_gb300 as mp
+        self.mp = mp
+        inp = make_inputs(name, T, seed=seed, device=dev)
+        wl = inp["wl"]
+        self.wl, self.T = wl, T
+        self.hidden, self.scales = inp["hidden"], inp["scales"]
+        self.ids, self.w, self.rows, self.emap = (inp["topk_ids"], inp["topk_weights"],
+                                                  inp["rows"], inp["expert_map"])
+        R = T * wl.K
+        self.offsets = torch.empty(wl.e_local + 1, dtype=torch.int64, device=dev)
+        self.pidx = torch.empty(R, dtype=torch.int32, device=dev)
+        self.inv = torch.empty(R, dtype=torch.int32, device=dev)
+        self.ph = torch.empty(R, wl.H, dtype=self.hidden.dtype, device=dev)
+        self.ps = None if self.scales is None else torch.empty(R, self.scales.shape[1],
+                                                               dtype=torch.float32, device=dev)
+        self.out = torch.empty(T, wl.H, dtype=torch.bfloat16, device=dev)
+        self.ws = torch.empty(mp.moe_permute_workspace_size(T, wl.K, wl.E), dtype=torch.uint8,
+                              device=dev)
+        mp.moe_permute_workspace_init(self.ws)
+        self.Tv, self.Nv = routing_counts(self.ids, self.emap, wl.E, wl.K)
+        elem = self.hidden.element_size()
+        sc = 0 if self.scales is None else self.scales.shape[1]
+        self.pbytes = permute_bytes(T, wl.H, wl.K, wl.e_local, elem, sc, self.Tv, self.Nv)
+        self.gbytes = gather_kernel_bytes(T, wl.H, wl.K, elem, sc, self.Tv, self.Nv)
+        self.ubytes = unpermute_bytes(T, wl.H, wl.K, self.Nv)
+
+    def permute(self):
+        self.mp.moe_permute(self.hidden, self.ids, self.offsets, self.pidx, self.inv, self.ws,
+                            num_experts=self.wl.E, num_local_experts=self.wl.e_local,
+                            expert_map=self.emap, hidden_scales=self.scales,
+                            permuted_hidden_states=self.ph, permuted_scales=self.ps)
+
+    def unpermute(self):
+        self.mp.moe_unpermute(self.rows, self.w, self.inv, self.out, workspace=self.ws)
+
+    def launches_per_permute(self):
+        return 1 if self.T * self.wl.K <= 8192 else 3
+
+
+def timed_calls(fn, n, flush=None):
+    """Mean device time (us) of fn over n calls, events around each call; the
+    L2 flush (if any) runs between calls, outside the events."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for i in range(n):
+        if flush is not None:
+            flush()
+        starts[i].record()
+        fn()
+        ends[i].record()
+    torch.cuda.synchronize()
+    return 1e3 * sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / n
+
+
+def graph_us(fn, n=100):
+    """Per-call time from replaying a CUDA graph of n back-to-back calls."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(n):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 5
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return 1e3 * a.elapsed_time(b) / (reps * n)
+
+
+def sweep(dev, peak, flush):
+    rows = []
+    for name, wl in WORKLOADS.items():
+        if name == "tiny":
+            continue
+        for T in wl.T_sweep:
+            s = Setup(name, T, seed=0, dev=dev)
+            for _ in range(3):
+                s.permute()
+                s.unpermute()
+            n = 30 if T >= 4096 else 100
+            p_us = timed_calls(s.permute, n, flush)
+            u_us = timed_calls(s.unpermute, n, flush)
+            rec = {"workload": name, "T": T,
+                   "permute_us": round(p_us, 2), "permute_GBps": round(s.pbytes / p_us / 1e3, 1),
+                   "permute_frac": round(s.pbytes / p_us / 1e3 / peak, 4),
+                   "unpermute_us": round(u_us, 2), "unpermute_GBps": round(s.ubytes / u_us / 1e3, 1),
+                   "unpermute_frac": round(s.ubytes / u_us / 1e3 / peak, 4)}
+            if T == 1:
+                rec["permute_graph_us"] = round(graph_us(s.permute), 2)
+                rec["unpermute_graph_us"] = round(graph_us(s.unpermute), 2)
+            rows.append(rec)
+            del s
+            torch.cuda.empty_cache()
+    return rows
+
+
+# ------------------------------------------------------------- CPU oracle ---
+class OracleStep:
+    """The CPU oracle (permute with the row copy, then unpermute) on the
+    headline workload's host inputs, optionally on its first T_sample tokens."""
+
+    def __init__(self):
+        import oracle
+        self.oracle = oracle
+        name, T = HEADLINE
+        inp = make_inputs(name, T, seed=0)
+        self.wl = inp["wl"]
+        self.T = T
+        self.ids_t = inp["topk_ids"]
+        self.ids = inp["topk_ids"].numpy()
+        self.hidden = inp["hidden"].view(torch.int16).numpy()
+        self.rows = inp["rows"].view(torch.int16).numpy().view(np.uint16)
+        self.w = inp["topk_weights"].numpy()
+
+    def nbytes(self, Ts):
+        wl = self.wl
+        Tv, Nv = routing_counts(self.ids_t[:Ts], None, wl.E, wl.K)
+        return permute_bytes(Ts, wl.H, wl.K, wl.e_local, 2, 0, Tv, Nv) + \
+            unpermute_bytes(Ts, wl.H, wl.K, Nv)
+
+    def run(self, Ts):
+        """One step on the first Ts tokens; returns its wall time in seconds."""
+        K = self.wl.K
+        t0 = time.perf_counter()
+        ref = self.oracle.permute(self.ids[:Ts], self.wl.E, hidden=self.hidden[:Ts])
+        self.oracle.unpermute(self.rows[:Ts * K], self.w[:Ts], ref["inv_permuted_idx"])
+        return time.perf_counter() - t0
+
+
+def cpu_baseline(budget_s=12.0):
+    """Repeat full-size oracle steps for about budget_s seconds of CPU work."""
+    o = OracleStep()
+    total, reps = 0.0, 0
+    while total < budget_s:
+        total += o.run(o.T)
+        reps += 1
+    per_step = total / reps
+    return {"value": round(o.nbytes(o.T) / per_step / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"mixtral T={o.T} H=4096 E=8 K=2: {reps} full oracle permute+unpermute "
+                      f"steps, {total:.1f} s of single-thread CPU work"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle as it stands, single-threaded, on the
+    headline workload; each step a sample of its first T_s tokens, sized so
+    warm-up plus timed steps stay within about two minutes."""
+    if rank != 0:
+        return
+    o = OracleStep()
+    t1 = o.run(o.T)
+    per_step_budget = 120.0 / (args.steps + args.warmup)
+    Ts = max(1, min(o.T, int(o.T * per_step_budget / t1)))
+    for _ in range(args.warmup):
+        o.run(Ts)
+    times = [o.run(Ts) for _ in range(args.steps)]
+    step_s = sum(times) / len(times)
+    value = o.nbytes(Ts) / step_s / 1e9
+    sample = (f"mixtral-shaped layer (H=4096, E=8, K=2), first {Ts} of {o.T} tokens per step: "
+              "one oracle permute (with row copy) + unpermute, single thread")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(step_s * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "mixtral-8x7b-moe-layer", "T": o.T, "T_sample": Ts,
+                       "H": 4096, "E": 8, "K": 2},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- main ---
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="own", choices=["own", "reference"])
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import moe_token_permute_gb300 as mp
+    mp._binding.lib()  # fails loudly if the CUDA library was not built
+    if not mp.moe_permute_supported(local):
+        raise SystemExit("this GPU is not an sm_103 device")
+
+    peak, peak_kind = measured_peak()
+    name, T = HEADLINE
+    sets = [Setup(name, T, seed=rank * 2 + i, dev=dev) for i in range(2)]
+    s0 = sets[0]
+    step_bytes = s0.pbytes + s0.ubytes
+    launches_per_step = s0.launches_per_permute() + 1
+
+    def step(i):
+        s = sets[i % 2]
+        s.permute()
+        s.unpermute()
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        start.record()
+        for i in range(n):
+            s = sets[i % 2]
+            ev[i][0].record()
+            s.permute()
+            ev[i][1].record()
+            s.unpermute()
+            ev[i][2].record()
+        end.record()
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    total_ms = start.elapsed_time(end)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / n
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    perm_us = 1e3 * sum(e[0].elapsed_time(e[1]) for e in ev) / n
+    unp_us = 1e3 * sum(e[1].elapsed_time(e[2]) for e in ev) / n
+
+    # end to end: pinned host inputs in, result out, every step
+    h_hidden = s0.hidden.cpu().pin_memory()
+    h_ids = s0.ids.cpu().pin_memory()
+    h_w = s0.w.cpu().pin_memory()
+    h_rows = s0.rows.cpu().pin_memory()
+    h_out = torch.empty_like(s0.out, device="cpu").pin_memory()
+    h_off = torch.empty_like(s0.offsets, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_hidden, h_ids, h_w, h_rows))
+    d2h = h_out.numel() * h_out.element_size() + h_off.numel() * h_off.element_size()
+
+    def e2e_step():
+        s0.hidden.copy_(h_hidden, non_blocking=True)
+        s0.ids.copy_(h_ids, non_blocking=True)
+        s0.w.copy_(h_w, non_blocking=True)
+        s0.rows.copy_(h_rows, non_blocking=True)
+        s0.permute()
+        s0.unpermute()
+        h_out.copy_(s0.out, non_blocking=True)
+        h_off.copy_(s0.offsets, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    n_e2e = min(n, 50)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(n_e2e):
+        e2e_step()
+    b.record()
+    torch.cuda.synchronize()
+    e2e_ms = a.elapsed_time(b) / n_e2e
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+
+    line = None
+    if rank == 0:
+        unp_gbs = s0.ubytes / unp_us / 1e3
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": n, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "mixtral-8x7b-moe-layer", "T": T, "H": s0.wl.H, "E": s0.wl.E,
+                       "K": s0.wl.K, "routing": "uniform distinct top-2",
+                       "parallelism": f"replicas x{world} (token batches, no collective)",
+                       "l2": f"inputs larger than L2: {step_bytes / 1e6:.0f} MB moved per step, "
+                             "two input sets alternate"},
+            "frac_of_peak": round(value / world / peak, 4),
+            "peak_GBps": peak, "peak_kind": peak_kind,
+            "bytes_per_step": step_bytes,
+            "permute": {"us_per_call": round(perm_us, 2), "GBps": round(s0.pbytes / perm_us / 1e3, 1),
+                        "frac": round(s0.pbytes / perm_us / 1e3 / peak, 4), "bytes": s0.pbytes,
+                        "launches": s0.launches_per_permute()},
+            "unpermute": {"us_per_call": round(unp_us, 2), "GBps": round(unp_gbs, 1),
+                          "frac": round(unp_gbs / peak, 4), "bytes": s0.ubytes, "launches": 1},
+            "roofline": {"kernel": "k_unpermute", "bound": "hbm", "achieved": round(unp_gbs, 1),
+                         "peak": peak, "unit": "GB/s", "frac": round(unp_gbs / peak, 4),
+                         "peak_kind": peak_kind,
+                         "traffic": ncu_traffic("k_unpermute", f"{name}-T{T}")},
+            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "steps": n_e2e},
+            "gpu_launches": n * launches_per_step,
+            "clocks": clk.summary(),
+        }
+    del h_hidden, h_rows
+    if rank == 0 and world == 1:
+        flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        if not args.no_sweep:
+            del sets, s0
+            torch.cuda.empty_cache()
+            line["sweep"] = sweep(dev, peak, flush=flush_buf.zero_)
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,202 @@
+/*
+ * moe_permute.h -- C ABI of the GB300 (sm_103a) MoE token permute / unpermute
+ * library (libmoe_permute.so).
+ *
+ * The two operations come from vLLM PR #14568, "permute/unpermute kernel for
+ * moe optimization", description: moe_permute expands every token into its K
+ * routed rows and orders them by expert, so that each expert's rows are
+ * contiguous for the grouped GEMM that follows; moe_unpermute reduces the
+ * expanded GEMM output back to tokens, scaling each row by its top-k weight.
+ * The output buffers and their shapes follow the vLLM PR #43014 digest,
+ * section "key source excerpts" (MoEPermuteScratch): expert_first_token_offset
+ * int64 [num_local_experts + 1], permuted_idx and inv_permuted_idx int32
+ * [max_tokens * topk], permuted_hidden_states [max_tokens * topk, hidden].
+ * The workspace-size query and the caller-owned, reused scratch follow the
+ * same digest, sections "implementation breakdown" (items 1 and 3: scratch
+ * allocated once and reused, the sort workspace sized by a query op) and
+ * "review highlights" (outputs are written into the caller's buffers, never
+ * into a copy).
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer except the ones noted as host pointers is a DEVICE pointer
+ *    to caller-owned, contiguous, row-major memory on the current device.
+ *    The library never allocates, frees or synchronises (except
+ *    moe_read_status, which synchronises the given stream by design); all
+ *    device work is enqueued on `stream` in stream order, so the calls can be
+ *    captured into a CUDA graph.
+ *  - Return value: MOE_OK (0) or a negative moe_status_t.  Argument errors are
+ *    detected on the host before anything is enqueued; nothing is written on
+ *    error.  No C++ exception crosses this ABI.
+ *  - Conditions found on the device (bad ids, bad map values, bad inverse
+ *    indices) never trap: the row is dropped and a MOE_FLAG_* bit is ORed into
+ *    the workspace status word (read it with moe_read_status).
+ *  - One workspace must not be used by two calls that may run concurrently
+ *    (two streams, or overlapping graph branches).
+ *  - Row order inside one expert is stable: key = local expert, tie-break =
+ *    expanded row id r = t*topk + k.
+ */
+#ifndef MOE_PERMUTE_H
+#define MOE_PERMUTE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,          /* bad size, NULL or misaligned pointer */
+    MOE_ERR_WORKSPACE_TOO_SMALL = -2,  /* workspace_bytes below the requirement */
+    MOE_ERR_UNSUPPORTED_DEVICE = -3,   /* current device is not sm_103 family */
+    MOE_ERR_CUDA = -4                  /* a CUDA runtime call or launch failed */
+} moe_status_t;
+
+/* Element type of the rows moved by moe_permute (rows are moved as bytes). */
+typedef enum {
+    MOE_DTYPE_BF16 = 0,
+    MOE_DTYPE_FP16 = 1,
+    MOE_DTYPE_FP8_E4M3 = 2,
+    MOE_DTYPE_FP8_E5M2 = 3,
+    MOE_DTYPE_FP32 = 4
+} moe_dtype_t;
+
+/* Storage type of topk_ids. */
+typedef enum { MOE_INDEX_INT32 = 0, MOE_INDEX_INT64 = 1 } moe_index_t;
+
+/* Device status bits (ORed into the workspace status word). */
+#define MOE_FLAG_ID_OUT_OF_RANGE  1u  /* a topk id outside [0, num_experts) */
+#define MOE_FLAG_MAP_OUT_OF_RANGE 2u  /* expert_map value not -1 and outside [0, num_local_experts) */
+#define MOE_FLAG_INV_OUT_OF_RANGE 4u  /* unpermute: inv index >= num_rows or < -1 */
+
+/* Limits checked on the host. */
+#define MOE_MAX_TOPK 32
+#define MOE_MAX_LOCAL_EXPERTS 1024
+
+/*
+ * moe_permute_supported: 1 if `device` is an sm_103-family GPU this library
+ * was built for, 0 if not, MOE_ERR_CUDA if the device cannot be queried.
+ * (Digest of vLLM PR #43014, "review highlights": callers check support
+ * before sizing the sort workspace.)
+ */
+MOE_API int moe_permute_supported(int device);
+
+/* Human-readable text for a moe_status_t; never NULL; static storage. */
+MOE_API const char *moe_status_string(int status);
+
+/*
+ * moe_permute_workspace_size: bytes of device workspace one moe_permute call
+ * with at most `max_tokens` tokens needs, for `topk` and `num_experts` (global
+ * experts).  Returns 0 for invalid arguments (max_tokens < 0, topk < 1 or
+ * > MOE_MAX_TOPK, num_experts < 1, or max_tokens*topk > INT32_MAX).
+ * The workspace holds per-block expert histograms, a completion ticket and
+ * the status word.  (Digest of vLLM PR #43014, "implementation breakdown"
+ * item 3: the sort workspace is sized by a query op and pre-allocated.)
+ */
+MOE_API size_t moe_permute_workspace_size(int64_t max_tokens, int32_t topk,
+                                  int32_t num_experts);
+
+/*
+ * moe_permute_workspace_init: zero the workspace's control words (ticket and
+ * status).  Call once after allocating the workspace (async on `stream`); every
+ * later call leaves the workspace ready for the next one.  `workspace` must be
+ * 256-byte aligned and at least moe_permute_workspace_size(...) bytes.
+ */
+MOE_API int moe_permute_workspace_init(void *workspace, size_t workspace_bytes,
+                               moe_stream_t stream);
+
+/*
+ * moe_permute: routing metadata plus the row gather.
+ *
+ *   T = num_tokens, H = hidden_size, K = topk, E = num_experts,
+ *   E_L = num_local_experts, R = T*K, r = t*K + k.
+ *
+ * In:
+ *  hidden_states     [T, H] of hidden_dtype.  May be NULL only when
+ *                    permuted_hidden_states is NULL (metadata-only call).
+ *  hidden_scales     [T, scale_cols] fp32 (e.g. fp8 per-token per-128-column
+ *                    scales, scale_cols = H/128) or NULL with scale_cols = 0.
+ *  topk_ids          [T, K], int32 or int64 per topk_ids_dtype (4/8-byte aligned).
+ *  expert_map        [E] int32 or NULL.  NULL: local expert = global id and
+ *                    E_L must equal E.  Otherwise expert_map[g] is the local id
+ *                    of global expert g, or -1 if g is not local (its rows are
+ *                    dropped).  Single-GPU index filtering only.
+ * Out (all written in place, stream-ordered):
+ *  permuted_hidden_states [R, H] or NULL.  Row p < N_valid is
+ *                    hidden_states[permuted_idx[p] / K]; rows >= N_valid are
+ *                    not written.
+ *  permuted_scales   [R, scale_cols] fp32, or NULL (must be NULL iff
+ *                    hidden_scales is NULL).  Row p is hidden_scales[token].
+ *  expert_first_token_offset [E_L + 1] int64 (8-byte aligned): offset[0] = 0,
+ *                    offset[e+1] - offset[e] = rows routed to local expert e,
+ *                    offset[E_L] = N_valid.
+ *  permuted_idx      [R] int32: p -> r for p < N_valid, -1 for p >= N_valid.
+ *  inv_permuted_idx  [R] int32: r -> p, or -1 for a dropped row.
+ * Workspace: at least moe_permute_workspace_size(T, K, E) bytes, 256-byte
+ *  aligned, initialised once by moe_permute_workspace_init.
+ * Dropped rows: an id outside [0, E) (flag MOE_FLAG_ID_OUT_OF_RANGE), a map
+ *  value of -1 (no flag), or a map value outside [0, E_L) other than -1
+ *  (flag MOE_FLAG_MAP_OUT_OF_RANGE).
+ * T = 0 is valid: offsets are set to 0 and nothing else is written.
+ * Limits: K <= MOE_MAX_TOPK, E_L <= MOE_MAX_LOCAL_EXPERTS, R <= INT32_MAX.
+ */
+MOE_API int moe_permute(const void *hidden_states, moe_dtype_t hidden_dtype,
+                const float *hidden_scales, int64_t scale_cols,
+                const void *topk_ids, moe_index_t topk_ids_dtype,
+                const int32_t *expert_map,
+                int64_t num_tokens, int64_t hidden_size, int32_t topk,
+                int32_t num_experts, int32_t num_local_experts,
+                void *permuted_hidden_states, float *permuted_scales,
+                int64_t *expert_first_token_offset,
+                int32_t *permuted_idx, int32_t *inv_permuted_idx,
+                void *workspace, size_t workspace_bytes,
+                moe_stream_t stream);
+
+/*
+ * moe_unpermute: out[t] = bf16_rne( sum over k = 0..K-1 in order, skipping
+ * rows with inv_permuted_idx[t*K+k] == -1, of topk_weights[t,k] *
+ * permuted_rows[inv_permuted_idx[t*K+k]] ), accumulated in fp32 with a
+ * separately rounded multiply and add per term.  A token whose rows were all
+ * dropped gets +0.0.
+ *
+ *  permuted_rows     [num_rows, H] bf16 (the grouped-GEMM output, in the
+ *                    permuted row order).
+ *  topk_weights      [T, K] fp32.
+ *  inv_permuted_idx  [T*K] int32, as written by moe_permute.  A value >=
+ *                    num_rows or < -1 is treated as dropped and, when a
+ *                    workspace is given, raises MOE_FLAG_INV_OUT_OF_RANGE.
+ *  out               [T, H] bf16.  Must not overlap the inputs.
+ *  workspace         optional (may be NULL): only its status word is used.
+ * T = 0 is valid and enqueues nothing.
+ */
+MOE_API int moe_unpermute(const void *permuted_rows, int64_t num_rows,
+                  const float *topk_weights, const int32_t *inv_permuted_idx,
+                  int64_t num_tokens, int64_t hidden_size, int32_t topk,
+                  void *out, void *workspace, moe_stream_t stream);
+
+/*
+ * moe_read_status: copy the workspace status word (OR of MOE_FLAG_* bits since
+ * the last clear) to the HOST pointer `host_status`.  Synchronises `stream`.
+ */
+MOE_API int moe_read_status(const void *workspace, uint32_t *host_status,
+                    moe_stream_t stream);
+
+/* moe_clear_status: zero the status word (async on `stream`). */
+MOE_API int moe_clear_status(void *workspace, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_PERMUTE_H */

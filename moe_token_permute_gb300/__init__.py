@@ -1,0 +1,206 @@
+"""GB300 (sm_103a) MoE token permute / unpermute behind a C ABI.
+
+The Python functions below carry the names of the C entry points declared in
+include/moe_permute.h and only marshal torch tensors into pointers and sizes;
+all work runs in libmoe_permute.so.  Every output buffer and the workspace are
+supplied by the caller, so no call allocates (vLLM PR #43014 digest,
+"implementation breakdown": scratch allocated once and reused).
+``MoEPermuteScratch`` allocates such a set of buffers once, up front.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+from . import _binding as _b
+from ._binding import (MOE_FLAG_ID_OUT_OF_RANGE, MOE_FLAG_INV_OUT_OF_RANGE,  # noqa: F401
+                       MOE_FLAG_MAP_OUT_OF_RANGE, MOE_MAX_LOCAL_EXPERTS, MOE_MAX_TOPK,
+                       MoeError, library_path)
+
+_DTYPES = {
+    torch.bfloat16: _b.MOE_DTYPE_BF16,
+    torch.float16: _b.MOE_DTYPE_FP16,
+    torch.float8_e4m3fn: _b.MOE_DTYPE_FP8_E4M3,
+    torch.float8_e5m2: _b.MOE_DTYPE_FP8_E5M2,
+    torch.float32: _b.MOE_DTYPE_FP32,
+}
+_INDEX = {torch.int32: _b.MOE_INDEX_INT32, torch.int64: _b.MOE_INDEX_INT64}
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor (the library writes in place)")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def moe_permute_supported(device: int | None = None) -> bool:
+    if device is None:
+        device = torch.cuda.current_device()
+    return _b.lib().moe_permute_supported(int(device)) == 1
+
+
+def moe_permute_workspace_size(max_tokens: int, topk: int, num_experts: int) -> int:
+    n = _b.lib().moe_permute_workspace_size(int(max_tokens), int(topk), int(num_experts))
+    if n == 0:
+        raise ValueError("invalid workspace size arguments")
+    return int(n)
+
+
+def moe_permute_workspace_init(workspace: torch.Tensor, stream=None) -> None:
+    _b.check("moe_permute_workspace_init",
+             _b.lib().moe_permute_workspace_init(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                                 _stream(stream)))
+
+
+def moe_permute(hidden_states, topk_ids, expert_first_token_offset, permuted_idx,
+                inv_permuted_idx, workspace, *, num_experts, num_local_experts=None,
+                expert_map=None, hidden_scales=None, permuted_hidden_states=None,
+                permuted_scales=None, stream=None) -> None:
+    """Permute in place into the given buffers (see include/moe_permute.h).
+
+    hidden_states [T,H] (None for a metadata-only call), topk_ids [T,K] int32
+    or int64, expert_first_token_offset int64 [E_local+1], permuted_idx and
+    inv_permuted_idx int32 [T*K], workspace uint8 (moe_permute_workspace_size),
+    permuted_hidden_states [T*K,H] or None, hidden_scales [T,S] fp32 and
+    permuted_scales [T*K,S] fp32 or both None.
+    """
+    T, K = topk_ids.shape
+    if num_local_experts is None:
+        num_local_experts = num_experts
+    if hidden_states is not None:
+        H = hidden_states.shape[1]
+        dt = _DTYPES[hidden_states.dtype]
+    else:
+        H, dt = 1, _b.MOE_DTYPE_BF16
+    scale_cols = hidden_scales.shape[1] if hidden_scales is not None else 0
+    _b.check("moe_permute", _b.lib().moe_permute(
+        _ptr(hidden_states), dt, _ptr(hidden_scales), scale_cols,
+        _ptr(topk_ids), _INDEX[topk_ids.dtype], _ptr(expert_map),
+        T, H, K, num_experts, num_local_experts,
+        _ptr(permuted_hidden_states), _ptr(permuted_scales),
+        _ptr(expert_first_token_offset), _ptr(permuted_idx), _ptr(inv_permuted_idx),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_unpermute(permuted_rows, topk_weights, inv_permuted_idx, out, *, workspace=None,
+                  stream=None) -> None:
+    """out[t] = bf16(sum_k w[t,k] * permuted_rows[inv[t*K+k]]) in place.
+
+    permuted_rows bf16 [num_rows,H], topk_weights fp32 [T,K], inv_permuted_idx
+    int32 [T*K], out bf16 [T,H]; workspace optional (status word only).
+    """
+    T, K = topk_weights.shape
+    H = out.shape[1]
+    if permuted_rows.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise ValueError("moe_unpermute takes bf16 rows and writes bf16")
+    if topk_weights.dtype != torch.float32 or inv_permuted_idx.dtype != torch.int32:
+        raise ValueError("topk_weights must be float32 and inv_permuted_idx int32")
+    if permuted_rows.shape[1] != H:
+        raise ValueError("hidden size mismatch between rows and out")
+    _b.check("moe_unpermute", _b.lib().moe_unpermute(
+        _ptr(permuted_rows), permuted_rows.shape[0], _ptr(topk_weights),
+        _ptr(inv_permuted_idx), T, H, K, _ptr(out), _ptr(workspace), _stream(stream)))
+
+
+def moe_read_status(workspace, stream=None) -> int:
+    """OR of the MOE_FLAG_* bits raised since the last clear (syncs the stream)."""
+    import ctypes
+    v = ctypes.c_uint32(0)
+    _b.check("moe_read_status", _b.lib().moe_read_status(_ptr(workspace), ctypes.byref(v),
+                                                        _stream(stream)))
+    return int(v.value)
+
+
+def moe_clear_status(workspace, stream=None) -> None:
+    _b.check("moe_clear_status", _b.lib().moe_clear_status(_ptr(workspace), _stream(stream)))
+
+
+@dataclass
+class MoEPermuteScratch:
+    """Buffers for repeated permutes, allocated once (vLLM PR #43014 digest,
+    "key source excerpts": MoEPermuteScratch.__post_init__ / validate).
+
+    Holds the workspace and the metadata buffers for up to max_num_tokens
+    tokens, plus permuted hidden (and fp8 scale) rows when hidden_size is given.
+    ``permute`` validates its inputs against these sizes and writes into views
+    of the same storage on every call.
+    """
+    max_num_tokens: int
+    topk: int
+    num_experts: int
+    num_local_experts: int
+    device: torch.device
+    hidden_size: int | None = None
+    hidden_dtype: torch.dtype | None = None
+    scale_cols: int = 0
+    workspace: torch.Tensor = field(init=False)
+    expert_first_token_offset: torch.Tensor = field(init=False)
+    permuted_idx: torch.Tensor = field(init=False)
+    inv_permuted_idx: torch.Tensor = field(init=False)
+    permuted_hidden_states: torch.Tensor | None = field(init=False, default=None)
+    permuted_scales: torch.Tensor | None = field(init=False, default=None)
+
+    def __post_init__(self):
+        dev = torch.device(self.device)
+        rows = self.max_num_tokens * self.topk
+        nbytes = moe_permute_workspace_size(self.max_num_tokens, self.topk, self.num_experts)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        moe_permute_workspace_init(self.workspace)
+        self.expert_first_token_offset = torch.empty(self.num_local_experts + 1,
+                                                     dtype=torch.int64, device=dev)
+        self.permuted_idx = torch.empty(rows, dtype=torch.int32, device=dev)
+        self.inv_permuted_idx = torch.empty(rows, dtype=torch.int32, device=dev)
+        if self.hidden_size is not None:
+            self.permuted_hidden_states = torch.empty(rows, self.hidden_size,
+                                                      dtype=self.hidden_dtype, device=dev)
+            if self.scale_cols:
+                self.permuted_scales = torch.empty(rows, self.scale_cols,
+                                                   dtype=torch.float32, device=dev)
+
+    def validate(self, hidden_states, topk_ids, hidden_scales=None):
+        n_token = topk_ids.shape[0]
+        if n_token > self.max_num_tokens:
+            raise ValueError(f"{n_token} tokens > max_num_tokens={self.max_num_tokens}")
+        if topk_ids.shape[1] != self.topk:
+            raise ValueError("topk mismatch")
+        if hidden_states is not None:
+            if hidden_states.shape[0] != n_token:
+                raise ValueError("hidden_states / topk_ids token count mismatch")
+            if self.hidden_size is not None and (hidden_states.shape[1] != self.hidden_size
+                                                 or hidden_states.dtype != self.hidden_dtype):
+                raise ValueError("hidden size / dtype mismatch")
+        if (hidden_scales is not None) != bool(self.scale_cols) and self.hidden_size is not None:
+            raise ValueError("scales given iff the scratch holds scale rows")
+
+    def permute(self, hidden_states, topk_ids, *, expert_map=None, hidden_scales=None,
+                stream=None):
+        """Permute into this scratch; returns views sized for this call."""
+        self.validate(hidden_states, topk_ids, hidden_scales)
+        n = topk_ids.shape[0] * self.topk
+        ph = None
+        ps = None
+        if self.permuted_hidden_states is not None and hidden_states is not None:
+            ph = self.permuted_hidden_states[:n]
+            if hidden_scales is not None:
+                ps = self.permuted_scales[:n]
+        moe_permute(hidden_states, topk_ids, self.expert_first_token_offset,
+                    self.permuted_idx[:n], self.inv_permuted_idx[:n], self.workspace,
+                    num_experts=self.num_experts, num_local_experts=self.num_local_experts,
+                    expert_map=expert_map, hidden_scales=hidden_scales,
+                    permuted_hidden_states=ph, permuted_scales=ps, stream=stream)
+        return dict(permuted_hidden_states=ph, permuted_scales=ps,
+                    expert_first_token_offset=self.expert_first_token_offset,
+                    permuted_idx=self.permuted_idx[:n], inv_permuted_idx=self.inv_permuted_idx[:n])

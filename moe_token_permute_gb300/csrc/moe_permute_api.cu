@@ -1,0 +1,364 @@
+// moe_permute_api.cu -- host side of the C ABI declared in include/moe_permute.h.
+//
+// Argument checks mirror MoEPermuteScratch.validate of the vLLM PR #43014
+// digest ("key source excerpts": token count within the pre-allocated maximum,
+// matching top-k, matching hidden size / dtype), returned as error codes.
+// Nothing here allocates: the caller owns every buffer, including the
+// workspace (same digest, "implementation breakdown" items 1-3).
+//
+// Dispatch:
+//   R = T*K <= kMetaChunkRows: one fused launch (k_permute_fused).
+//   otherwise: k_route_hist -> k_route_scatter -> k_gather_rows, chained with
+//   programmatic dependent launch so each grid's launch latency overlaps the
+//   previous grid's tail.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "moe_permute.h"
+#include "common.cuh"
+#include "routing.cuh"
+#include "rows.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int cc_major = 0;
+  int cc_minor = 0;
+  int sm_count = 0;
+  int max_smem_optin = 0;
+};
+
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+
+// Cached properties of the current device; nullptr if it cannot be queried.
+const DeviceInfo* current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+      return nullptr;
+    d.ready = true;
+  }
+  return &d;
+}
+
+bool is_supported(const DeviceInfo* d) { return d != nullptr && d->cc_major == 10 && d->cc_minor == 3; }
+
+// Raise a kernel's dynamic shared memory limit once per device.
+template <typename Kern>
+cudaError_t allow_smem(Kern kern, size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  return cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+}
+
+// Launch with programmatic stream serialization: the grid may be scheduled as
+// soon as the previous grid in the stream allows it; every kernel here calls
+// griddepcontrol.wait before it touches memory a previous grid may write.
+template <typename... KArgs, typename... Args>
+cudaError_t launch(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                   cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Widest vector (16/8/4/2/1 bytes) that divides the row pitch and both bases.
+size_t vec_bytes(int64_t row_bytes, const void* a, const void* b) {
+  for (size_t w = 16; w > 1; w >>= 1)
+    if (row_bytes % static_cast<int64_t>(w) == 0 && aligned(a, w) && (b == nullptr || aligned(b, w)))
+      return w;
+  return 1;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+size_t workspace_bytes_for(int64_t max_tokens, int32_t topk, int32_t num_experts) {
+  const int64_t R = max_tokens * topk;
+  const int64_t blocks = std::max<int64_t>(1, ceil_div(R, kMetaChunkRows));
+  size_t bytes = kWsHeaderBytes + static_cast<size_t>(num_experts) * static_cast<size_t>(blocks) * 4;
+  return (bytes + 255) / 256 * 256;
+}
+
+constexpr int kGatherV = 8;     // 16-byte vectors per lane in flight (gather)
+constexpr int kFusedV = 4;      // same, inside the 1024-thread fused kernel
+constexpr int kUnpermuteV = 2;  // 16-byte vectors per lane per k step (unpermute)
+
+// Grid for a warp-per-token kernel: enough warps for every token, capped at a
+// few waves of resident blocks.
+unsigned token_grid(int64_t T, int warps_per_block, const DeviceInfo* d, int blocks_per_sm) {
+  const int64_t need = ceil_div(T, warps_per_block);
+  const int64_t cap = static_cast<int64_t>(d->sm_count) * blocks_per_sm;
+  return static_cast<unsigned>(std::max<int64_t>(1, std::min(need, cap)));
+}
+
+template <typename IdT, typename VecT, int V>
+cudaError_t launch_fused(const IdT* ids, const int32_t* emap, int64_t T, int K, int E, int E_local,
+                         const void* hidden, int64_t row_bytes, const float* scales,
+                         int64_t scale_cols, void* out, float* out_scales, int64_t* offsets,
+                         int32_t* pidx, int32_t* inv, WsHeader* hdr, const DeviceInfo* d,
+                         cudaStream_t s) {
+  const int64_t R = T * K;
+  const size_t smem = (static_cast<size_t>(kMetaWarps) * E_local + E_local + 1 + R) * sizeof(int);
+  auto kern = k_permute_fused<IdT, VecT, V>;
+  cudaError_t err = allow_smem(kern, smem);
+  if (err != cudaSuccess) return err;
+  const unsigned grid = out == nullptr ? 1u : token_grid(T, kMetaWarps, d, 1);
+  return launch(kern, grid, kMetaThreads, smem, s, ids, emap, T, K, E, E_local,
+                static_cast<const VecT*>(hidden), row_bytes / static_cast<int64_t>(sizeof(VecT)),
+                scales, scale_cols, static_cast<VecT*>(out), out_scales, offsets, pidx, inv, hdr);
+}
+
+template <typename VecT, int V>
+cudaError_t launch_gather(const void* hidden, int64_t row_bytes, const float* scales,
+                          int64_t scale_cols, const int32_t* inv, int64_t T, int K, void* out,
+                          float* out_scales, const DeviceInfo* d, cudaStream_t s) {
+  const unsigned grid = token_grid(T, kRowThreads / kWarpSize, d, 8);
+  return launch(k_gather_rows<VecT, V>, grid, kRowThreads, 0, s, static_cast<const VecT*>(hidden),
+                row_bytes / static_cast<int64_t>(sizeof(VecT)), scales, scale_cols, inv, T, K,
+                static_cast<VecT*>(out), out_scales);
+}
+
+template <typename IdT>
+cudaError_t permute_typed(const IdT* ids, const int32_t* emap, int64_t T, int K, int E,
+                          int E_local, const void* hidden, int64_t row_bytes, const float* scales,
+                          int64_t scale_cols, void* out, float* out_scales, int64_t* offsets,
+                          int32_t* pidx, int32_t* inv, void* ws, const DeviceInfo* d,
+                          cudaStream_t s) {
+  WsHeader* hdr = static_cast<WsHeader*>(ws);
+  const int64_t R = T * K;
+  const size_t vb = out == nullptr ? 16 : vec_bytes(row_bytes, hidden, out);
+  if (R <= kMetaChunkRows) {
+    switch (vb) {
+      case 16: return launch_fused<IdT, uint4, kFusedV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
+      case 8: return launch_fused<IdT, uint2, kFusedV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
+      case 4: return launch_fused<IdT, uint32_t, kFusedV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
+      case 2: return launch_fused<IdT, uint16_t, kFusedV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
+      default: return launch_fused<IdT, uint8_t, kFusedV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
+    }
+  }
+  const unsigned B = static_cast<unsigned>(ceil_div(R, kMetaChunkRows));
+  int* hist = reinterpret_cast<int*>(static_cast<char*>(ws) + kWsHeaderBytes);
+  const size_t smem_hist = static_cast<size_t>(E_local) * sizeof(int);
+  const size_t smem_scatter = (static_cast<size_t>(kMetaWarps) + 1) * E_local * sizeof(int);
+  cudaError_t err = allow_smem(k_route_scatter<IdT>, smem_scatter);
+  if (err != cudaSuccess) return err;
+  err = launch(k_route_hist<IdT>, B, kMetaThreads, smem_hist, s, ids, emap, R, E, E_local, hist,
+               offsets, hdr);
+  if (err != cudaSuccess) return err;
+  err = launch(k_route_scatter<IdT>, B, kMetaThreads, smem_scatter, s, ids, emap, R, E, E_local,
+               static_cast<const int*>(hist), static_cast<const int64_t*>(offsets), pidx, inv);
+  if (err != cudaSuccess || out == nullptr) return err;
+  switch (vb) {
+    case 16: return launch_gather<uint4, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, d, s);
+    case 8: return launch_gather<uint2, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, d, s);
+    case 4: return launch_gather<uint32_t, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, d, s);
+    case 2: return launch_gather<uint16_t, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, d, s);
+    default: return launch_gather<uint8_t, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, d, s);
+  }
+}
+
+template <typename VecT>
+cudaError_t launch_unpermute(const void* rows, int64_t num_rows, int64_t H, const float* w,
+                             const int32_t* inv, int64_t T, int K, void* out, unsigned* status,
+                             const DeviceInfo* d, cudaStream_t s) {
+  const int64_t row_vecs = H * 2 / static_cast<int64_t>(sizeof(VecT));
+  const unsigned grid = token_grid(T, kRowThreads / kWarpSize, d, 8);
+  return launch(k_unpermute<VecT, kUnpermuteV>, grid, kRowThreads, 0, s,
+                static_cast<const VecT*>(rows), num_rows, row_vecs, w, inv, T, K,
+                static_cast<VecT*>(out), status);
+}
+
+int elem_bytes(moe_dtype_t dt) {
+  switch (dt) {
+    case MOE_DTYPE_BF16:
+    case MOE_DTYPE_FP16: return 2;
+    case MOE_DTYPE_FP8_E4M3:
+    case MOE_DTYPE_FP8_E5M2: return 1;
+    case MOE_DTYPE_FP32: return 4;
+    default: return 0;
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_permute_supported(int device) {
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return (major == 10 && minor == 3) ? 1 : 0;
+}
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103)";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown status";
+  }
+}
+
+size_t moe_permute_workspace_size(int64_t max_tokens, int32_t topk, int32_t num_experts) {
+  if (max_tokens < 0 || topk < 1 || topk > MOE_MAX_TOPK || num_experts < 1) return 0;
+  if (max_tokens > INT32_MAX / topk) return 0;
+  return workspace_bytes_for(max_tokens, topk, num_experts);
+}
+
+int moe_permute_workspace_init(void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < kWsHeaderBytes)
+    return MOE_ERR_INVALID_ARG;
+  if (!is_supported(current_device())) return MOE_ERR_UNSUPPORTED_DEVICE;
+  if (cudaMemsetAsync(workspace, 0, kWsHeaderBytes, reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_permute(const void* hidden_states, moe_dtype_t hidden_dtype, const float* hidden_scales,
+                int64_t scale_cols, const void* topk_ids, moe_index_t topk_ids_dtype,
+                const int32_t* expert_map, int64_t num_tokens, int64_t hidden_size, int32_t topk,
+                int32_t num_experts, int32_t num_local_experts, void* permuted_hidden_states,
+                float* permuted_scales, int64_t* expert_first_token_offset, int32_t* permuted_idx,
+                int32_t* inv_permuted_idx, void* workspace, size_t workspace_bytes,
+                moe_stream_t stream) {
+  const int eb = elem_bytes(hidden_dtype);
+  const int64_t T = num_tokens, H = hidden_size;
+  if (eb == 0 || T < 0 || H < 1 || topk < 1 || topk > MOE_MAX_TOPK || num_experts < 1 ||
+      num_local_experts < 1 || num_local_experts > num_experts ||
+      num_local_experts > MOE_MAX_LOCAL_EXPERTS)
+    return MOE_ERR_INVALID_ARG;
+  if (expert_map == nullptr && num_local_experts != num_experts) return MOE_ERR_INVALID_ARG;
+  if (topk_ids_dtype != MOE_INDEX_INT32 && topk_ids_dtype != MOE_INDEX_INT64)
+    return MOE_ERR_INVALID_ARG;
+  if (T > INT32_MAX / topk) return MOE_ERR_INVALID_ARG;
+  if (H > INT64_MAX / 16 / eb) return MOE_ERR_INVALID_ARG;
+  const size_t id_bytes = topk_ids_dtype == MOE_INDEX_INT64 ? 8 : 4;
+  if (topk_ids == nullptr || !aligned(topk_ids, id_bytes)) return MOE_ERR_INVALID_ARG;
+  if (expert_map != nullptr && !aligned(expert_map, 4)) return MOE_ERR_INVALID_ARG;
+  if (expert_first_token_offset == nullptr || !aligned(expert_first_token_offset, 8))
+    return MOE_ERR_INVALID_ARG;
+  if (permuted_idx == nullptr || inv_permuted_idx == nullptr || !aligned(permuted_idx, 4) ||
+      !aligned(inv_permuted_idx, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (permuted_hidden_states != nullptr && hidden_states == nullptr) return MOE_ERR_INVALID_ARG;
+  const bool with_scales = hidden_scales != nullptr || permuted_scales != nullptr;
+  if (with_scales) {
+    if (hidden_scales == nullptr || permuted_scales == nullptr || scale_cols < 1 ||
+        permuted_hidden_states == nullptr || !aligned(hidden_scales, 4) ||
+        !aligned(permuted_scales, 4))
+      return MOE_ERR_INVALID_ARG;
+  } else if (scale_cols != 0) {
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (workspace == nullptr || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < workspace_bytes_for(T, topk, num_experts))
+    return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const DeviceInfo* d = current_device();
+  if (!is_supported(d)) return MOE_ERR_UNSUPPORTED_DEVICE;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (T == 0) {
+    err = launch(k_zero_offsets, 1, 256, 0, s, expert_first_token_offset, num_local_experts + 1);
+  } else if (topk_ids_dtype == MOE_INDEX_INT32) {
+    err = permute_typed<int32_t>(static_cast<const int32_t*>(topk_ids), expert_map, T, topk,
+                                 num_experts, num_local_experts, hidden_states, H * eb,
+                                 hidden_scales, scale_cols, permuted_hidden_states,
+                                 permuted_scales, expert_first_token_offset, permuted_idx,
+                                 inv_permuted_idx, workspace, d, s);
+  } else {
+    err = permute_typed<int64_t>(static_cast<const int64_t*>(topk_ids), expert_map, T, topk,
+                                 num_experts, num_local_experts, hidden_states, H * eb,
+                                 hidden_scales, scale_cols, permuted_hidden_states,
+                                 permuted_scales, expert_first_token_offset, permuted_idx,
+                                 inv_permuted_idx, workspace, d, s);
+  }
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_unpermute(const void* permuted_rows, int64_t num_rows, const float* topk_weights,
+                  const int32_t* inv_permuted_idx, int64_t num_tokens, int64_t hidden_size,
+                  int32_t topk, void* out, void* workspace, moe_stream_t stream) {
+  const int64_t T = num_tokens, H = hidden_size;
+  if (T < 0 || H < 1 || topk < 1 || topk > MOE_MAX_TOPK || num_rows < 0) return MOE_ERR_INVALID_ARG;
+  if (T > INT32_MAX / topk || num_rows > INT32_MAX || H > INT64_MAX / 32)
+    return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (permuted_rows == nullptr && num_rows > 0) return MOE_ERR_INVALID_ARG;
+  if (topk_weights == nullptr || inv_permuted_idx == nullptr || out == nullptr ||
+      !aligned(topk_weights, 4) || !aligned(inv_permuted_idx, 4) || !aligned(out, 2) ||
+      (permuted_rows != nullptr && !aligned(permuted_rows, 2)))
+    return MOE_ERR_INVALID_ARG;
+  if (workspace != nullptr && !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+  const DeviceInfo* d = current_device();
+  if (!is_supported(d)) return MOE_ERR_UNSUPPORTED_DEVICE;
+  unsigned* status = workspace != nullptr ? &static_cast<WsHeader*>(workspace)->status : nullptr;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t vb = vec_bytes(H * 2, permuted_rows != nullptr ? permuted_rows : out, out);
+  cudaError_t err;
+  switch (vb) {
+    case 16: err = launch_unpermute<uint4>(permuted_rows, num_rows, H, topk_weights, inv_permuted_idx, T, topk, out, status, d, s); break;
+    case 8: err = launch_unpermute<uint2>(permuted_rows, num_rows, H, topk_weights, inv_permuted_idx, T, topk, out, status, d, s); break;
+    case 4: err = launch_unpermute<uint32_t>(permuted_rows, num_rows, H, topk_weights, inv_permuted_idx, T, topk, out, status, d, s); break;
+    default: err = launch_unpermute<uint16_t>(permuted_rows, num_rows, H, topk_weights, inv_permuted_idx, T, topk, out, status, d, s); break;
+  }
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_read_status(const void* workspace, uint32_t* host_status, moe_stream_t stream) {
+  if (workspace == nullptr || host_status == nullptr || !aligned(workspace, 256))
+    return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const void* src = &static_cast<const WsHeader*>(workspace)->status;
+  if (cudaMemcpyAsync(host_status, src, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_clear_status(void* workspace, moe_stream_t stream) {
+  if (workspace == nullptr || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+  void* dst = &static_cast<WsHeader*>(workspace)->status;
+  if (cudaMemsetAsync(dst, 0, sizeof(uint32_t), reinterpret_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,252 @@
+// rows.cuh -- the row-moving kernels of moe_permute and moe_unpermute.
+//
+// vLLM PR #14568 ("permute/unpermute kernel for moe optimization",
+// description): permute gathers each expert's non-contiguous tokens into
+// contiguous rows for the grouped GEMM; unpermute reduces the expanded GEMM
+// output back to tokens and scales each row by its top-k weight.
+//
+// Both are pure HBM traffic.  A warp owns one token at a time: permute reads
+// the token's row once and writes it to each of its K destinations;
+// unpermute reads the token's K rows and writes one.  Rows move in VecT-wide
+// vectors (16 bytes when pointers and the row pitch allow), V vectors per lane
+// in flight per chunk.
+#pragma once
+
+#include "common.cuh"
+#include "routing.cuh"
+
+namespace moe {
+
+constexpr int kRowThreads = 256;
+
+// Copy one token's row (row_vecs vectors) to every destination row p_k whose
+// bit k is set in `valid`; lane k < K holds p_k in `p_lane`.
+template <typename VecT, int V>
+__device__ __forceinline__ void copy_token_rows(const VecT* __restrict__ src, int64_t row_vecs,
+                                                VecT* __restrict__ out, int p_lane,
+                                                unsigned valid) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t c0 = 0; c0 < row_vecs; c0 += 32 * V) {
+    VecT v[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int64_t c = c0 + i * 32 + lane;
+      if (c < row_vecs) v[i] = ld_stream(src + c);
+    }
+    unsigned m = valid;
+    while (m != 0u) {
+      const int k = __ffs(m) - 1;
+      m &= m - 1u;
+      const int pk = __shfl_sync(kFullMask, p_lane, k);
+      VecT* dst = out + static_cast<int64_t>(pk) * row_vecs;
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int64_t c = c0 + i * 32 + lane;
+        if (c < row_vecs) dst[c] = v[i];
+      }
+    }
+  }
+}
+
+// Copy one token's fp32 scale row (scale_cols floats) to its destinations.
+__device__ __forceinline__ void copy_token_scales(const float* __restrict__ src, int64_t scale_cols,
+                                                  float* __restrict__ out, int p_lane,
+                                                  unsigned valid) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t c0 = 0; c0 < scale_cols; c0 += 32) {
+    const int64_t c = c0 + lane;
+    const float s = c < scale_cols ? __ldg(src + c) : 0.f;
+    unsigned m = valid;
+    while (m != 0u) {
+      const int k = __ffs(m) - 1;
+      m &= m - 1u;
+      const int pk = __shfl_sync(kFullMask, p_lane, k);
+      if (c < scale_cols) out[static_cast<int64_t>(pk) * scale_cols + c] = s;
+    }
+  }
+}
+
+// Kernel 3: row gather driven by inv_permuted_idx (written by kernel 2).
+template <typename VecT, int V>
+__global__ void __launch_bounds__(kRowThreads)
+k_gather_rows(const VecT* __restrict__ hidden, int64_t row_vecs,
+              const float* __restrict__ scales, int64_t scale_cols,
+              const int32_t* __restrict__ inv_permuted_idx, int64_t T, int K,
+              VecT* __restrict__ permuted_hidden, float* __restrict__ permuted_scales) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t t = warp0; t < T; t += n_warps) {
+    const int p = lane < K ? __ldcg(inv_permuted_idx + t * K + lane) : -1;
+    const unsigned valid = __ballot_sync(kFullMask, p >= 0);
+    if (valid == 0u) continue;  // every row of this token was dropped
+    copy_token_rows<VecT, V>(hidden + t * row_vecs, row_vecs, permuted_hidden, p, valid);
+    if (permuted_scales != nullptr)
+      copy_token_scales(scales + t * scale_cols, scale_cols, permuted_scales, p, valid);
+  }
+}
+
+// Single-launch permute for R <= kMetaChunkRows expanded rows.  Every block
+// computes the whole stable counting sort in shared memory (R is small, the
+// ids come from L2), block 0 writes the metadata, and all blocks share the
+// row copy: no block ever waits for another.
+// Shared memory: cnt [kMetaWarps][E_local] | s_base [E_local + 1] | s_p [R].
+template <typename IdT, typename VecT, int V>
+__global__ void __launch_bounds__(kMetaThreads)
+k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
+                int64_t T, int K, int E, int E_local,
+                const VecT* __restrict__ hidden, int64_t row_vecs,
+                const float* __restrict__ scales, int64_t scale_cols,
+                VecT* __restrict__ permuted_hidden, float* __restrict__ permuted_scales,
+                int64_t* __restrict__ offsets, int32_t* __restrict__ permuted_idx,
+                int32_t* __restrict__ inv_permuted_idx, WsHeader* __restrict__ hdr) {
+  extern __shared__ int smem[];
+  __shared__ int s_warp[32];
+  int* cnt = smem;
+  int* s_base = cnt + kMetaWarps * E_local;
+  int* s_p = s_base + E_local + 1;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t R = T * K;
+  const bool writer = blockIdx.x == 0;
+
+  pdl_wait();
+  for (int i = threadIdx.x; i < kMetaWarps * E_local; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+
+  const int64_t slice0 = static_cast<int64_t>(warp) * 32 * kMetaRowsPerLane;
+  int key[kMetaRowsPerLane], rank[kMetaRowsPerLane];
+  unsigned flags = 0;
+  load_keys<IdT, kMetaRowsPerLane>(ids, emap, E, E_local, slice0, R, key, flags);
+  rank_warp_slice<kMetaRowsPerLane>(key, cnt + warp * E_local, rank);
+  if (writer) {
+    flags = __reduce_or_sync(kFullMask, flags);
+    if (flags != 0 && lane == 0) atomicOr(&hdr->status, flags);
+  }
+  __syncthreads();
+  scan_counts_over_warps(cnt, E_local, s_base);
+  __syncthreads();
+  // Exclusive scan of the per-expert totals (E_local <= blockDim.x).
+  {
+    const int v = threadIdx.x < E_local ? s_base[threadIdx.x] : 0;
+    int total;
+    const int excl = block_exclusive_sum(v, s_warp, &total);
+    if (threadIdx.x < E_local) s_base[threadIdx.x] = excl;
+    if (threadIdx.x == 0) s_base[E_local] = total;
+  }
+  __syncthreads();
+  if (writer)
+    for (int e = threadIdx.x; e <= E_local; e += blockDim.x) offsets[e] = s_base[e];
+
+#pragma unroll
+  for (int j = 0; j < kMetaRowsPerLane; ++j) {
+    const int64_t r = slice0 + j * 32 + lane;
+    if (r < R) {
+      const int e = key[j];
+      const int p = e >= 0 ? s_base[e] + cnt[warp * E_local + e] + rank[j] : -1;
+      s_p[r] = p;
+      if (writer) {
+        inv_permuted_idx[r] = p;
+        if (p >= 0) permuted_idx[p] = static_cast<int32_t>(r);
+      }
+    }
+  }
+  if (writer)
+    for (int64_t p = s_base[E_local] + threadIdx.x; p < R; p += blockDim.x) permuted_idx[p] = -1;
+  if (permuted_hidden == nullptr) return;
+  __syncthreads();
+
+  const int64_t n_warps = static_cast<int64_t>(gridDim.x) * kMetaWarps;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kMetaWarps + warp; t < T; t += n_warps) {
+    const int p = lane < K ? s_p[t * K + lane] : -1;
+    const unsigned valid = __ballot_sync(kFullMask, p >= 0);
+    if (valid == 0u) continue;
+    copy_token_rows<VecT, V>(hidden + t * row_vecs, row_vecs, permuted_hidden, p, valid);
+    if (permuted_scales != nullptr)
+      copy_token_scales(scales + t * scale_cols, scale_cols, permuted_scales, p, valid);
+  }
+}
+
+// bf16 lanes (raw bits) of a vector register.
+template <typename VecT>
+struct Bf16Vec {
+  static constexpr int kElems = sizeof(VecT) / 2;
+  union {
+    VecT v;
+    unsigned short e[kElems];
+  };
+};
+
+// Unpermute: warp per token, k in ascending order, fp32 multiply then fp32
+// add per term (no contraction), one bf16 round-to-nearest-even at the end.
+template <typename VecT, int V>
+__global__ void __launch_bounds__(kRowThreads)
+k_unpermute(const VecT* __restrict__ rows, int64_t num_rows, int64_t row_vecs,
+            const float* __restrict__ topk_weights, const int32_t* __restrict__ inv_permuted_idx,
+            int64_t T, int K, VecT* __restrict__ out, unsigned* __restrict__ status) {
+  constexpr int kE = Bf16Vec<VecT>::kElems;
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t t = warp0; t < T; t += n_warps) {
+    int p = -1;
+    float w = 0.f;
+    bool bad = false;
+    if (lane < K) {
+      p = __ldg(inv_permuted_idx + t * K + lane);
+      w = __ldg(topk_weights + t * K + lane);
+      if (p < -1 || p >= num_rows) {
+        bad = true;
+        p = -1;
+      }
+    }
+    if (status != nullptr && __any_sync(kFullMask, bad) && lane == 0)
+      atomicOr(status, MOE_FLAG_INV_OUT_OF_RANGE);
+    const unsigned valid = __ballot_sync(kFullMask, p >= 0);
+    for (int64_t c0 = 0; c0 < row_vecs; c0 += 32 * V) {
+      float acc[V][kE];
+#pragma unroll
+      for (int i = 0; i < V; ++i)
+#pragma unroll
+        for (int e = 0; e < kE; ++e) acc[i][e] = 0.f;
+      for (int k = 0; k < K; ++k) {
+        if (((valid >> k) & 1u) == 0u) continue;
+        const int pk = __shfl_sync(kFullMask, p, k);
+        const float wk = __shfl_sync(kFullMask, w, k);
+        const VecT* src = rows + static_cast<int64_t>(pk) * row_vecs;
+        Bf16Vec<VecT> x[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+          const int64_t c = c0 + i * 32 + lane;
+          if (c < row_vecs) x[i].v = ld_stream(src + c);
+        }
+#pragma unroll
+        for (int i = 0; i < V; ++i)
+#pragma unroll
+          for (int e = 0; e < kE; ++e)
+            acc[i][e] = __fadd_rn(acc[i][e],
+                                  __fmul_rn(wk, __bfloat162float(__ushort_as_bfloat16(x[i].e[e]))));
+      }
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int64_t c = c0 + i * 32 + lane;
+        if (c < row_vecs) {
+          Bf16Vec<VecT> y;
+#pragma unroll
+          for (int e = 0; e < kE; ++e) y.e[e] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i][e]));
+          out[t * row_vecs + c] = y.v;
+        }
+      }
+    }
+  }
+}
+
+// T = 0: offsets all zero.
+__global__ void k_zero_offsets(int64_t* __restrict__ offsets, int n) {
+  pdl_wait();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) offsets[i] = 0;
+}
+
+}  // namespace moe

@@ -1,0 +1,126 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol the
+header declares, and its host-only entry points (workspace sizing, status
+text, argument checks that run before any device work) behave as declared."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from moe_token_permute_gb300 import _binding as b
+from moe_token_permute_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return b.lib()
+
+
+def declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        with open(h) as f:
+            text = f.read()
+        names |= set(re.findall(r"MOE_API\s+[\w\s\*]*?\b(moe_\w+)\s*\(", text))
+    return names
+
+
+def test_header_declares_entry_points():
+    names = declared_symbols()
+    for n in ("moe_permute_workspace_size", "moe_permute", "moe_unpermute",
+              "moe_permute_workspace_init", "moe_permute_supported"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+        assert n in b.SIGNATURES, f"{n} has no ctypes signature in the binding"
+
+
+def test_library_built_for_sm103a_only():
+    src = open(cuda_build.__file__).read()
+    assert "arch=compute_103a,code=sm_103a" in src
+
+
+def test_workspace_size(lib):
+    ws = lib.moe_permute_workspace_size
+    assert ws(0, 1, 1) == 256 + 256  # header + one (padded) histogram block
+    a = ws(4096, 2, 8)
+    c = ws(32768, 8, 256)
+    assert a % 256 == 0 and c % 256 == 0
+    # 32768*8 rows = 32 chunks of 8192 rows; one int per (expert, chunk)
+    assert c == 256 + 256 * 32 * 4
+    assert ws(100, 8, 256) <= c  # monotone in tokens
+    assert ws(-1, 2, 8) == 0
+    assert ws(16, 0, 8) == 0
+    assert ws(16, 33, 8) == 0
+    assert ws(16, 2, 0) == 0
+    assert ws(2**31, 2, 8) == 0  # T*K beyond int32
+
+
+def test_status_strings(lib):
+    assert lib.moe_status_string(0) == b"ok"
+    assert b"workspace" in lib.moe_status_string(-2)
+    assert lib.moe_status_string(12345) == b"unknown status"
+
+
+def _permute_args(**over):
+    # a structurally valid call with fake (never dereferenced) device pointers
+    args = dict(hidden=0x1000, dt=b.MOE_DTYPE_BF16, scales=None, scale_cols=0,
+                ids=0x2000, idt=b.MOE_INDEX_INT32, emap=None, T=4, H=8, K=2, E=4, EL=4,
+                out=0x3000, out_scales=None, offsets=0x4000, pidx=0x5000, inv=0x6000,
+                ws=0x10000, ws_bytes=1 << 20, stream=None)
+    args.update(over)
+    return list(args.values())
+
+
+@pytest.mark.parametrize("over", [
+    dict(K=0), dict(K=33), dict(E=0), dict(EL=5), dict(EL=2),  # EL != E without a map
+    dict(EL=1025, E=2000, emap=0x7000), dict(T=-1), dict(H=0), dict(dt=9), dict(idt=3),
+    dict(ids=None), dict(ids=0x2002), dict(offsets=0x4004), dict(pidx=None), dict(inv=0x6002),
+    dict(hidden=None), dict(scales=0x8000), dict(scale_cols=3), dict(ws=None),
+    dict(ws=0x10010), dict(T=2**30, K=4),
+])
+def test_permute_rejects_bad_arguments_on_host(lib, over):
+    assert lib.moe_permute(*_permute_args(**over)) == b.MOE_ERR_INVALID_ARG
+
+
+def test_permute_workspace_too_small(lib):
+    assert lib.moe_permute(*_permute_args(T=100000, ws_bytes=512)) == b.MOE_ERR_WORKSPACE_TOO_SMALL
+
+
+@pytest.mark.parametrize("args", [
+    (0x1000, 4, 0x2000, 0x3000, 4, 8, 0, 0x4000, None, None),   # K = 0
+    (0x1000, 4, 0x2000, 0x3000, 4, 8, 40, 0x4000, None, None),  # K > 32
+    (0x1000, 4, 0x2000, 0x3000, 4, 0, 2, 0x4000, None, None),   # H = 0
+    (0x1000, 4, None, 0x3000, 4, 8, 2, 0x4000, None, None),     # weights NULL
+    (0x1000, 4, 0x2000, 0x3000, 4, 8, 2, 0x4001, None, None),   # out misaligned
+    (0x1000, 4, 0x2000, 0x3000, 4, 8, 2, 0x4000, 0x10010, None),  # ws misaligned
+])
+def test_unpermute_rejects_bad_arguments_on_host(lib, args):
+    assert lib.moe_unpermute(*args) == b.MOE_ERR_INVALID_ARG
+
+
+def test_unpermute_empty_batch_is_a_no_op(lib):
+    assert lib.moe_unpermute(None, 0, None, None, 0, 8, 2, None, None, None) == b.MOE_OK
+
+
+def test_status_calls_reject_bad_workspace(lib):
+    v = ctypes.c_uint32(0)
+    assert lib.moe_read_status(None, ctypes.byref(v), None) == b.MOE_ERR_INVALID_ARG
+    assert lib.moe_clear_status(0x10010, None) == b.MOE_ERR_INVALID_ARG
+    assert lib.moe_permute_workspace_init(0x10000, 16, None) == b.MOE_ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        b.lib()
