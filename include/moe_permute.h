@@ -148,7 +148,8 @@ MOE_API int moe_permute_workspace_init(void *workspace, size_t workspace_bytes,
  * Dropped rows: an id outside [0, E) (flag MOE_FLAG_ID_OUT_OF_RANGE), a map
  *  value of -1 (no flag), or a map value outside [0, E_L) other than -1
  *  (flag MOE_FLAG_MAP_OUT_OF_RANGE).
- * T = 0 is valid: offsets are set to 0 and nothing else is written.
+ * T = 0 is valid: offsets are set to 0 and nothing else is written; every
+ *  pointer but expert_first_token_offset may then be NULL.
  * Limits: K <= MOE_MAX_TOPK, E_L <= MOE_MAX_LOCAL_EXPERTS, R <= INT32_MAX.
  */
 MOE_API int moe_permute(const void *hidden_states, moe_dtype_t hidden_dtype,

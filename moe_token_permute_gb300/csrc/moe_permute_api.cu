@@ -106,15 +106,36 @@ size_t workspace_bytes_for(int64_t max_tokens, int32_t topk, int32_t num_experts
   return (bytes + 255) / 256 * 256;
 }
 
-constexpr int kGatherV = 8;     // 16-byte vectors per lane in flight (gather)
+constexpr int kGatherV = 8;     // vectors per lane in one gather chunk
 constexpr int kFusedV = 4;      // same, inside the 1024-thread fused kernel
-constexpr int kUnpermuteV = 2;  // 16-byte vectors per lane per k step (unpermute)
+constexpr int kUnpermuteV = 2;  // vectors per lane in one unpermute chunk
 
-// Grid for a warp-per-token kernel: enough warps for every token, capped at a
-// few waves of resident blocks.
-unsigned token_grid(int64_t T, int warps_per_block, const DeviceInfo* d, int blocks_per_sm) {
-  const int64_t need = ceil_div(T, warps_per_block);
-  const int64_t cap = static_cast<int64_t>(d->sm_count) * blocks_per_sm;
+// (token, chunk) work items of a row kernel.
+int64_t row_items(int64_t T, int64_t row_vecs, int V) {
+  return T * std::max<int64_t>(1, ceil_div(row_vecs, 32 * static_cast<int64_t>(V)));
+}
+
+// Resident blocks per SM of a kernel (queried once per device and kernel).
+template <typename Kern>
+int blocks_per_sm(Kern kern, int threads, size_t smem) {
+  static int cache[kMaxDevices] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess || n < 1)
+      n = 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+// Grid for a warp-per-item kernel: one warp per item, capped at one wave of
+// resident blocks (the kernels loop over items).
+unsigned item_grid(int64_t items, int warps_per_block, const DeviceInfo* d, int per_sm) {
+  const int64_t need = ceil_div(items, warps_per_block);
+  const int64_t cap = static_cast<int64_t>(d->sm_count) * per_sm;
   return static_cast<unsigned>(std::max<int64_t>(1, std::min(need, cap)));
 }
 
@@ -125,11 +146,14 @@ cudaError_t launch_fused(const IdT* ids, const int32_t* emap, int64_t T, int K, 
                          int32_t* pidx, int32_t* inv, WsHeader* hdr, const DeviceInfo* d,
                          cudaStream_t s) {
   const int64_t R = T * K;
-  const size_t smem = (static_cast<size_t>(kMetaWarps) * E_local + E_local + 1 + R) * sizeof(int);
+  const int64_t rank_warps = ceil_div(R, 32 * kMetaRowsPerLane);
+  const size_t smem = (static_cast<size_t>(rank_warps) * E_local + E_local + 1 + R) * sizeof(int);
   auto kern = k_permute_fused<IdT, VecT, V>;
   cudaError_t err = allow_smem(kern, smem);
   if (err != cudaSuccess) return err;
-  const unsigned grid = out == nullptr ? 1u : token_grid(T, kMetaWarps, d, 1);
+  const int64_t row_vecs = row_bytes / static_cast<int64_t>(sizeof(VecT));
+  const unsigned grid =
+      out == nullptr ? 1u : item_grid(row_items(T, row_vecs, V), kMetaWarps, d, 1);
   return launch(kern, grid, kMetaThreads, smem, s, ids, emap, T, K, E, E_local,
                 static_cast<const VecT*>(hidden), row_bytes / static_cast<int64_t>(sizeof(VecT)),
                 scales, scale_cols, static_cast<VecT*>(out), out_scales, offsets, pidx, inv, hdr);
@@ -139,10 +163,12 @@ template <typename VecT, int V>
 cudaError_t launch_gather(const void* hidden, int64_t row_bytes, const float* scales,
                           int64_t scale_cols, const int32_t* inv, int64_t T, int K, void* out,
                           float* out_scales, const DeviceInfo* d, cudaStream_t s) {
-  const unsigned grid = token_grid(T, kRowThreads / kWarpSize, d, 8);
-  return launch(k_gather_rows<VecT, V>, grid, kRowThreads, 0, s, static_cast<const VecT*>(hidden),
-                row_bytes / static_cast<int64_t>(sizeof(VecT)), scales, scale_cols, inv, T, K,
-                static_cast<VecT*>(out), out_scales);
+  const int64_t row_vecs = row_bytes / static_cast<int64_t>(sizeof(VecT));
+  auto kern = k_gather_rows<VecT, V>;
+  const unsigned grid = item_grid(row_items(T, row_vecs, V), kRowWarps, d,
+                                  blocks_per_sm(kern, kRowThreads, 0));
+  return launch(kern, grid, kRowThreads, 0, s, static_cast<const VecT*>(hidden), row_vecs, scales,
+                scale_cols, inv, T, K, static_cast<VecT*>(out), out_scales);
 }
 
 template <typename IdT>
@@ -189,10 +215,11 @@ cudaError_t launch_unpermute(const void* rows, int64_t num_rows, int64_t H, cons
                              const int32_t* inv, int64_t T, int K, void* out, unsigned* status,
                              const DeviceInfo* d, cudaStream_t s) {
   const int64_t row_vecs = H * 2 / static_cast<int64_t>(sizeof(VecT));
-  const unsigned grid = token_grid(T, kRowThreads / kWarpSize, d, 8);
-  return launch(k_unpermute<VecT, kUnpermuteV>, grid, kRowThreads, 0, s,
-                static_cast<const VecT*>(rows), num_rows, row_vecs, w, inv, T, K,
-                static_cast<VecT*>(out), status);
+  auto kern = k_unpermute<VecT, kUnpermuteV>;
+  const unsigned grid = item_grid(row_items(T, row_vecs, kUnpermuteV), kRowWarps, d,
+                                  blocks_per_sm(kern, kRowThreads, 0));
+  return launch(kern, grid, kRowThreads, 0, s, static_cast<const VecT*>(rows), num_rows, row_vecs,
+                w, inv, T, K, static_cast<VecT*>(out), status);
 }
 
 int elem_bytes(moe_dtype_t dt) {
@@ -268,27 +295,31 @@ int moe_permute(const void* hidden_states, moe_dtype_t hidden_dtype, const float
     return MOE_ERR_INVALID_ARG;
   if (T > INT32_MAX / topk) return MOE_ERR_INVALID_ARG;
   if (H > INT64_MAX / 16 / eb) return MOE_ERR_INVALID_ARG;
-  const size_t id_bytes = topk_ids_dtype == MOE_INDEX_INT64 ? 8 : 4;
-  if (topk_ids == nullptr || !aligned(topk_ids, id_bytes)) return MOE_ERR_INVALID_ARG;
-  if (expert_map != nullptr && !aligned(expert_map, 4)) return MOE_ERR_INVALID_ARG;
   if (expert_first_token_offset == nullptr || !aligned(expert_first_token_offset, 8))
     return MOE_ERR_INVALID_ARG;
-  if (permuted_idx == nullptr || inv_permuted_idx == nullptr || !aligned(permuted_idx, 4) ||
-      !aligned(inv_permuted_idx, 4))
-    return MOE_ERR_INVALID_ARG;
-  if (permuted_hidden_states != nullptr && hidden_states == nullptr) return MOE_ERR_INVALID_ARG;
-  const bool with_scales = hidden_scales != nullptr || permuted_scales != nullptr;
-  if (with_scales) {
-    if (hidden_scales == nullptr || permuted_scales == nullptr || scale_cols < 1 ||
-        permuted_hidden_states == nullptr || !aligned(hidden_scales, 4) ||
-        !aligned(permuted_scales, 4))
+  if (scale_cols < 0) return MOE_ERR_INVALID_ARG;
+  // With T = 0 only the offsets are written; empty tensors may come as NULL.
+  if (T > 0) {
+    const size_t id_bytes = topk_ids_dtype == MOE_INDEX_INT64 ? 8 : 4;
+    if (topk_ids == nullptr || !aligned(topk_ids, id_bytes)) return MOE_ERR_INVALID_ARG;
+    if (expert_map != nullptr && !aligned(expert_map, 4)) return MOE_ERR_INVALID_ARG;
+    if (permuted_idx == nullptr || inv_permuted_idx == nullptr || !aligned(permuted_idx, 4) ||
+        !aligned(inv_permuted_idx, 4))
       return MOE_ERR_INVALID_ARG;
-  } else if (scale_cols != 0) {
-    return MOE_ERR_INVALID_ARG;
+    if (permuted_hidden_states != nullptr && hidden_states == nullptr) return MOE_ERR_INVALID_ARG;
+    const bool with_scales = hidden_scales != nullptr || permuted_scales != nullptr;
+    if (with_scales) {
+      if (hidden_scales == nullptr || permuted_scales == nullptr || scale_cols < 1 ||
+          permuted_hidden_states == nullptr || !aligned(hidden_scales, 4) ||
+          !aligned(permuted_scales, 4))
+        return MOE_ERR_INVALID_ARG;
+    } else if (scale_cols != 0) {
+      return MOE_ERR_INVALID_ARG;
+    }
+    if (workspace == nullptr || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < workspace_bytes_for(T, topk, num_experts))
+      return MOE_ERR_WORKSPACE_TOO_SMALL;
   }
-  if (workspace == nullptr || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
-  if (workspace_bytes < workspace_bytes_for(T, topk, num_experts))
-    return MOE_ERR_WORKSPACE_TOO_SMALL;
   const DeviceInfo* d = current_device();
   if (!is_supported(d)) return MOE_ERR_UNSUPPORTED_DEVICE;
 

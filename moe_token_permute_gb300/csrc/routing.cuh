@@ -86,13 +86,14 @@ __device__ __forceinline__ void rank_warp_slice(const int (&key)[J], int* cnt_w,
   }
 }
 
-// Turn cnt[w][e] (w < kMetaWarps) into exclusive prefixes over w, in place;
+// Turn cnt[w][e] (w < n_warps) into exclusive prefixes over w, in place;
 // s_total[e] receives the block's count of expert e.
-__device__ __forceinline__ void scan_counts_over_warps(int* cnt, int E_local, int* s_total) {
+__device__ __forceinline__ void scan_counts_over_warps(int* cnt, int E_local, int n_warps,
+                                                       int* s_total) {
   for (int e = threadIdx.x; e < E_local; e += blockDim.x) {
     int run = 0;
 #pragma unroll 8
-    for (int w = 0; w < kMetaWarps; ++w) {
+    for (int w = 0; w < n_warps; ++w) {
       const int c = cnt[w * E_local + e];
       cnt[w * E_local + e] = run;
       run += c;
@@ -196,7 +197,7 @@ k_route_scatter(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
   load_keys<IdT, kMetaRowsPerLane>(ids, emap, E, E_local, slice0, row_end, key, flags);
   rank_warp_slice<kMetaRowsPerLane>(key, cnt + warp * E_local, rank);
   __syncthreads();
-  scan_counts_over_warps(cnt, E_local, s_base);  // s_base used as scratch for totals
+  scan_counts_over_warps(cnt, E_local, kMetaWarps, s_base);  // s_base: scratch for totals
 
   pdl_wait();  // kernel 1's bases and offsets are visible from here on
   pdl_launch_dependents();

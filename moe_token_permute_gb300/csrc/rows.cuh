@@ -5,11 +5,14 @@
 // contiguous rows for the grouped GEMM; unpermute reduces the expanded GEMM
 // output back to tokens and scales each row by its top-k weight.
 //
-// Both are pure HBM traffic.  A warp owns one token at a time: permute reads
-// the token's row once and writes it to each of its K destinations;
-// unpermute reads the token's K rows and writes one.  Rows move in VecT-wide
-// vectors (16 bytes when pointers and the row pitch allow), V vectors per lane
-// in flight per chunk.
+// Both are pure HBM traffic.  The unit of work is a (token, chunk) item: one
+// warp moves one chunk of 32*V vectors of one token's row (VecT is 16 bytes
+// whenever the pointers and the row pitch allow it).  Permute reads the chunk
+// once and writes it to each of the token's K destinations; unpermute reads
+// the chunk of each of the token's kept rows -- all loads of a group of up to
+// four rows in flight at once -- and writes one.  Splitting rows into chunks
+// keeps every SM busy at small token counts and bounds the registers per warp
+// at large ones.
 #pragma once
 
 #include "common.cuh"
@@ -18,32 +21,36 @@
 namespace moe {
 
 constexpr int kRowThreads = 256;
+constexpr int kRowWarps = kRowThreads / kWarpSize;
 
-// Copy one token's row (row_vecs vectors) to every destination row p_k whose
-// bit k is set in `valid`; lane k < K holds p_k in `p_lane`.
 template <typename VecT, int V>
-__device__ __forceinline__ void copy_token_rows(const VecT* __restrict__ src, int64_t row_vecs,
-                                                VecT* __restrict__ out, int p_lane,
-                                                unsigned valid) {
+__device__ __forceinline__ void load_chunk(const VecT* __restrict__ src, int64_t c0,
+                                           int64_t row_vecs, VecT (&v)[V]) {
   const int lane = threadIdx.x & 31;
-  for (int64_t c0 = 0; c0 < row_vecs; c0 += 32 * V) {
-    VecT v[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int64_t c = c0 + i * 32 + lane;
+    if (c < row_vecs) v[i] = ld_stream(src + c);
+  }
+}
+
+// Write one chunk to every destination row p_k whose bit k is set in `valid`;
+// lane k < K holds p_k in `p_lane`.
+template <typename VecT, int V>
+__device__ __forceinline__ void store_chunk(const VecT (&v)[V], VecT* __restrict__ out,
+                                            int64_t c0, int64_t row_vecs, int p_lane,
+                                            unsigned valid) {
+  const int lane = threadIdx.x & 31;
+  unsigned m = valid;
+  while (m != 0u) {
+    const int k = __ffs(m) - 1;
+    m &= m - 1u;
+    const int pk = __shfl_sync(kFullMask, p_lane, k);
+    VecT* dst = out + static_cast<int64_t>(pk) * row_vecs;
 #pragma unroll
     for (int i = 0; i < V; ++i) {
       const int64_t c = c0 + i * 32 + lane;
-      if (c < row_vecs) v[i] = ld_stream(src + c);
-    }
-    unsigned m = valid;
-    while (m != 0u) {
-      const int k = __ffs(m) - 1;
-      m &= m - 1u;
-      const int pk = __shfl_sync(kFullMask, p_lane, k);
-      VecT* dst = out + static_cast<int64_t>(pk) * row_vecs;
-#pragma unroll
-      for (int i = 0; i < V; ++i) {
-        const int64_t c = c0 + i * 32 + lane;
-        if (c < row_vecs) dst[c] = v[i];
-      }
+      if (c < row_vecs) dst[c] = v[i];
     }
   }
 }
@@ -67,22 +74,43 @@ __device__ __forceinline__ void copy_token_scales(const float* __restrict__ src,
 }
 
 // Kernel 3: row gather driven by inv_permuted_idx (written by kernel 2).
+// The grid starts once the routing kernels have passed their own dependency
+// waits, so the caller's hidden rows are complete: each warp loads its first
+// chunk before waiting for the index maps, overlapping that load with the tail
+// of the routing kernels.
 template <typename VecT, int V>
 __global__ void __launch_bounds__(kRowThreads)
 k_gather_rows(const VecT* __restrict__ hidden, int64_t row_vecs,
               const float* __restrict__ scales, int64_t scale_cols,
               const int32_t* __restrict__ inv_permuted_idx, int64_t T, int K,
               VecT* __restrict__ permuted_hidden, float* __restrict__ permuted_scales) {
-  pdl_wait();
+  constexpr int64_t kChunk = 32 * V;
   const int lane = threadIdx.x & 31;
+  const int64_t n_chunks = (row_vecs + kChunk - 1) / kChunk;
+  const int64_t n_items = T * n_chunks;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t t = warp0; t < T; t += n_warps) {
+  VecT v[V];
+  bool have = false;
+  if (warp0 < n_items) {
+    const int64_t t = warp0 / n_chunks;
+    load_chunk<VecT, V>(hidden + t * row_vecs, (warp0 - t * n_chunks) * kChunk, row_vecs, v);
+    have = true;
+  }
+  pdl_wait();
+  for (int64_t item = warp0; item < n_items; item += n_warps) {
+    const int64_t t = item / n_chunks;
+    const int64_t c0 = (item - t * n_chunks) * kChunk;
     const int p = lane < K ? __ldcg(inv_permuted_idx + t * K + lane) : -1;
     const unsigned valid = __ballot_sync(kFullMask, p >= 0);
-    if (valid == 0u) continue;  // every row of this token was dropped
-    copy_token_rows<VecT, V>(hidden + t * row_vecs, row_vecs, permuted_hidden, p, valid);
-    if (permuted_scales != nullptr)
+    if (valid == 0u) {  // every row of this token was dropped
+      have = false;
+      continue;
+    }
+    if (!have) load_chunk<VecT, V>(hidden + t * row_vecs, c0, row_vecs, v);
+    have = false;
+    store_chunk<VecT, V>(v, permuted_hidden, c0, row_vecs, p, valid);
+    if (permuted_scales != nullptr && c0 == 0)
       copy_token_scales(scales + t * scale_cols, scale_cols, permuted_scales, p, valid);
   }
 }
@@ -91,9 +119,9 @@ k_gather_rows(const VecT* __restrict__ hidden, int64_t row_vecs,
 // computes the whole stable counting sort in shared memory (R is small, the
 // ids come from L2), block 0 writes the metadata, and all blocks share the
 // row copy: no block ever waits for another.
-// Shared memory: cnt [kMetaWarps][E_local] | s_base [E_local + 1] | s_p [R].
+// Shared memory: cnt [n_rank_warps][E_local] | s_base [E_local + 1] | s_p [R].
 template <typename IdT, typename VecT, int V>
-__global__ void __launch_bounds__(kMetaThreads)
+__global__ void __launch_bounds__(kMetaThreads, 1)
 k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
                 int64_t T, int K, int E, int E_local,
                 const VecT* __restrict__ hidden, int64_t row_vecs,
@@ -103,29 +131,33 @@ k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
                 int32_t* __restrict__ inv_permuted_idx, WsHeader* __restrict__ hdr) {
   extern __shared__ int smem[];
   __shared__ int s_warp[32];
+  const int64_t R = T * K;
+  // warps that own at least one row (each owns 32 * kMetaRowsPerLane rows)
+  const int n_rank_warps = static_cast<int>((R + 32 * kMetaRowsPerLane - 1) / (32 * kMetaRowsPerLane));
   int* cnt = smem;
-  int* s_base = cnt + kMetaWarps * E_local;
+  int* s_base = cnt + n_rank_warps * E_local;
   int* s_p = s_base + E_local + 1;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int64_t R = T * K;
   const bool writer = blockIdx.x == 0;
 
   pdl_wait();
-  for (int i = threadIdx.x; i < kMetaWarps * E_local; i += blockDim.x) cnt[i] = 0;
+  for (int i = threadIdx.x; i < n_rank_warps * E_local; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
 
   const int64_t slice0 = static_cast<int64_t>(warp) * 32 * kMetaRowsPerLane;
   int key[kMetaRowsPerLane], rank[kMetaRowsPerLane];
-  unsigned flags = 0;
-  load_keys<IdT, kMetaRowsPerLane>(ids, emap, E, E_local, slice0, R, key, flags);
-  rank_warp_slice<kMetaRowsPerLane>(key, cnt + warp * E_local, rank);
-  if (writer) {
-    flags = __reduce_or_sync(kFullMask, flags);
-    if (flags != 0 && lane == 0) atomicOr(&hdr->status, flags);
+  if (warp < n_rank_warps) {
+    unsigned flags = 0;
+    load_keys<IdT, kMetaRowsPerLane>(ids, emap, E, E_local, slice0, R, key, flags);
+    rank_warp_slice<kMetaRowsPerLane>(key, cnt + warp * E_local, rank);
+    if (writer) {
+      flags = __reduce_or_sync(kFullMask, flags);
+      if (flags != 0 && lane == 0) atomicOr(&hdr->status, flags);
+    }
   }
   __syncthreads();
-  scan_counts_over_warps(cnt, E_local, s_base);
+  scan_counts_over_warps(cnt, E_local, n_rank_warps, s_base);
   __syncthreads();
   // Exclusive scan of the per-expert totals (E_local <= blockDim.x).
   {
@@ -139,16 +171,18 @@ k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
   if (writer)
     for (int e = threadIdx.x; e <= E_local; e += blockDim.x) offsets[e] = s_base[e];
 
+  if (warp < n_rank_warps) {
 #pragma unroll
-  for (int j = 0; j < kMetaRowsPerLane; ++j) {
-    const int64_t r = slice0 + j * 32 + lane;
-    if (r < R) {
-      const int e = key[j];
-      const int p = e >= 0 ? s_base[e] + cnt[warp * E_local + e] + rank[j] : -1;
-      s_p[r] = p;
-      if (writer) {
-        inv_permuted_idx[r] = p;
-        if (p >= 0) permuted_idx[p] = static_cast<int32_t>(r);
+    for (int j = 0; j < kMetaRowsPerLane; ++j) {
+      const int64_t r = slice0 + j * 32 + lane;
+      if (r < R) {
+        const int e = key[j];
+        const int p = e >= 0 ? s_base[e] + cnt[warp * E_local + e] + rank[j] : -1;
+        s_p[r] = p;
+        if (writer) {
+          inv_permuted_idx[r] = p;
+          if (p >= 0) permuted_idx[p] = static_cast<int32_t>(r);
+        }
       }
     }
   }
@@ -157,13 +191,21 @@ k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
   if (permuted_hidden == nullptr) return;
   __syncthreads();
 
+  constexpr int64_t kChunk = 32 * V;
+  const int64_t n_chunks = (row_vecs + kChunk - 1) / kChunk;
+  const int64_t n_items = T * n_chunks;
   const int64_t n_warps = static_cast<int64_t>(gridDim.x) * kMetaWarps;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * kMetaWarps + warp; t < T; t += n_warps) {
+  for (int64_t item = static_cast<int64_t>(blockIdx.x) * kMetaWarps + warp; item < n_items;
+       item += n_warps) {
+    const int64_t t = item / n_chunks;
+    const int64_t c0 = (item - t * n_chunks) * kChunk;
     const int p = lane < K ? s_p[t * K + lane] : -1;
     const unsigned valid = __ballot_sync(kFullMask, p >= 0);
     if (valid == 0u) continue;
-    copy_token_rows<VecT, V>(hidden + t * row_vecs, row_vecs, permuted_hidden, p, valid);
-    if (permuted_scales != nullptr)
+    VecT v[V];
+    load_chunk<VecT, V>(hidden + t * row_vecs, c0, row_vecs, v);
+    store_chunk<VecT, V>(v, permuted_hidden, c0, row_vecs, p, valid);
+    if (permuted_scales != nullptr && c0 == 0)
       copy_token_scales(scales + t * scale_cols, scale_cols, permuted_scales, p, valid);
   }
 }
@@ -178,7 +220,9 @@ struct Bf16Vec {
   };
 };
 
-// Unpermute: warp per token, k in ascending order, fp32 multiply then fp32
+constexpr int kUnpermuteGroup = 4;  // kept rows whose loads are in flight together
+
+// Unpermute: warp per (token, chunk).  k ascending, fp32 multiply then fp32
 // add per term (no contraction), one bf16 round-to-nearest-even at the end.
 template <typename VecT, int V>
 __global__ void __launch_bounds__(kRowThreads)
@@ -186,11 +230,17 @@ k_unpermute(const VecT* __restrict__ rows, int64_t num_rows, int64_t row_vecs,
             const float* __restrict__ topk_weights, const int32_t* __restrict__ inv_permuted_idx,
             int64_t T, int K, VecT* __restrict__ out, unsigned* __restrict__ status) {
   constexpr int kE = Bf16Vec<VecT>::kElems;
+  constexpr int kG = kUnpermuteGroup;
+  constexpr int64_t kChunk = 32 * V;
   pdl_wait();
   const int lane = threadIdx.x & 31;
+  const int64_t n_chunks = (row_vecs + kChunk - 1) / kChunk;
+  const int64_t n_items = T * n_chunks;
   const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  for (int64_t t = warp0; t < T; t += n_warps) {
+  for (int64_t item = warp0; item < n_items; item += n_warps) {
+    const int64_t t = item / n_chunks;
+    const int64_t c0 = (item - t * n_chunks) * kChunk;
     int p = -1;
     float w = 0.f;
     bool bad = false;
@@ -202,42 +252,53 @@ k_unpermute(const VecT* __restrict__ rows, int64_t num_rows, int64_t row_vecs,
         p = -1;
       }
     }
-    if (status != nullptr && __any_sync(kFullMask, bad) && lane == 0)
+    if (status != nullptr && c0 == 0 && __any_sync(kFullMask, bad) && lane == 0)
       atomicOr(status, MOE_FLAG_INV_OUT_OF_RANGE);
-    const unsigned valid = __ballot_sync(kFullMask, p >= 0);
-    for (int64_t c0 = 0; c0 < row_vecs; c0 += 32 * V) {
-      float acc[V][kE];
+    float acc[V][kE];
 #pragma unroll
-      for (int i = 0; i < V; ++i)
+    for (int i = 0; i < V; ++i)
 #pragma unroll
-        for (int e = 0; e < kE; ++e) acc[i][e] = 0.f;
-      for (int k = 0; k < K; ++k) {
-        if (((valid >> k) & 1u) == 0u) continue;
-        const int pk = __shfl_sync(kFullMask, p, k);
-        const float wk = __shfl_sync(kFullMask, w, k);
+      for (int e = 0; e < kE; ++e) acc[i][e] = 0.f;
+    unsigned m = __ballot_sync(kFullMask, p >= 0);  // kept rows, k ascending
+    while (m != 0u) {
+      int ks[kG];
+#pragma unroll
+      for (int j = 0; j < kG; ++j) {
+        ks[j] = m != 0u ? __ffs(m) - 1 : -1;
+        m &= m - 1u;  // no-op once m is 0
+      }
+      Bf16Vec<VecT> x[kG][V];
+#pragma unroll
+      for (int j = 0; j < kG; ++j) {
+        if (ks[j] < 0) continue;
+        const int pk = __shfl_sync(kFullMask, p, ks[j]);
         const VecT* src = rows + static_cast<int64_t>(pk) * row_vecs;
-        Bf16Vec<VecT> x[V];
 #pragma unroll
         for (int i = 0; i < V; ++i) {
           const int64_t c = c0 + i * 32 + lane;
-          if (c < row_vecs) x[i].v = ld_stream(src + c);
+          if (c < row_vecs) x[j][i].v = ld_stream(src + c);
         }
+      }
+#pragma unroll
+      for (int j = 0; j < kG; ++j) {
+        if (ks[j] < 0) continue;
+        const float wk = __shfl_sync(kFullMask, w, ks[j]);
 #pragma unroll
         for (int i = 0; i < V; ++i)
 #pragma unroll
           for (int e = 0; e < kE; ++e)
-            acc[i][e] = __fadd_rn(acc[i][e],
-                                  __fmul_rn(wk, __bfloat162float(__ushort_as_bfloat16(x[i].e[e]))));
+            acc[i][e] = __fadd_rn(
+                acc[i][e], __fmul_rn(wk, __bfloat162float(__ushort_as_bfloat16(x[j][i].e[e]))));
       }
+    }
 #pragma unroll
-      for (int i = 0; i < V; ++i) {
-        const int64_t c = c0 + i * 32 + lane;
-        if (c < row_vecs) {
-          Bf16Vec<VecT> y;
+    for (int i = 0; i < V; ++i) {
+      const int64_t c = c0 + i * 32 + lane;
+      if (c < row_vecs) {
+        Bf16Vec<VecT> y;
 #pragma unroll
-          for (int e = 0; e < kE; ++e) y.e[e] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i][e]));
-          out[t * row_vecs + c] = y.v;
-        }
+        for (int e = 0; e < kE; ++e) y.e[e] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i][e]));
+        out[t * row_vecs + c] = y.v;
       }
     }
   }

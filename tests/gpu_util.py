@@ -25,7 +25,8 @@ def bits16(t: torch.Tensor) -> np.ndarray:
 def bytes_of(t: torch.Tensor) -> np.ndarray:
     """Any tensor -> its raw bytes [rows, row_bytes] on the host."""
     t = t.detach().cpu().contiguous()
-    return t.view(torch.uint8).numpy().reshape(t.shape[0], -1)
+    row_bytes = t.element_size() * (t[0].numel() if t.dim() > 1 else 1)
+    return t.view(torch.uint8).numpy().reshape(t.shape[0], row_bytes)
 
 
 def alloc_outputs(T, K, E_local, H=None, dtype=None, scale_cols=0, E=None, device=DEV):
