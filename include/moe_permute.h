@@ -79,6 +79,8 @@ typedef enum { MOE_INDEX_INT32 = 0, MOE_INDEX_INT64 = 1 } moe_index_t;
 #define MOE_FLAG_ID_OUT_OF_RANGE  1u  /* a topk id outside [0, num_experts) */
 #define MOE_FLAG_MAP_OUT_OF_RANGE 2u  /* expert_map value not -1 and outside [0, num_local_experts) */
 #define MOE_FLAG_INV_OUT_OF_RANGE 4u  /* unpermute: inv index >= num_rows or < -1 */
+#define MOE_FLAG_BARRIER_TIMEOUT  8u  /* permute: a bounded grid-barrier wait gave up
+                                         (outputs of that call are undefined) */
 
 /* Limits checked on the host. */
 #define MOE_MAX_TOPK 32

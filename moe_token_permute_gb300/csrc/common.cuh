@@ -16,7 +16,9 @@ constexpr unsigned kFullMask = 0xffffffffu;
 struct WsHeader {
   unsigned ticket;  // blocks of the histogram kernel that have finished
   unsigned status;  // OR of MOE_FLAG_* bits
-  unsigned reserved[62];
+  unsigned arrive;  // grid barrier: blocks arrived (the last one resets it)
+  unsigned gen;     // grid barrier: generation, bumped once per barrier
+  unsigned reserved[60];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 constexpr size_t kWsHeaderBytes = sizeof(WsHeader);

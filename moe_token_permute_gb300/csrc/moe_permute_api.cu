@@ -22,6 +22,7 @@
 #include "common.cuh"
 #include "routing.cuh"
 #include "rows.cuh"
+#include "permute_coop.cuh"
 
 namespace moe {
 namespace {
@@ -99,16 +100,22 @@ size_t vec_bytes(int64_t row_bytes, const void* a, const void* b) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+constexpr int64_t kCoopMaxBlocks = 1024;  // table rows reserved for the cooperative grid
+
 size_t workspace_bytes_for(int64_t max_tokens, int32_t topk, int32_t num_experts) {
   const int64_t R = max_tokens * topk;
-  const int64_t blocks = std::max<int64_t>(1, ceil_div(R, kMetaChunkRows));
-  size_t bytes = kWsHeaderBytes + static_cast<size_t>(num_experts) * static_cast<size_t>(blocks) * 4;
+  const int64_t hist_blocks = std::max<int64_t>(1, ceil_div(R, kMetaChunkRows));
+  const int64_t e_pad = (num_experts + 3) / 4 * 4;
+  const int64_t coop_blocks = std::max<int64_t>(1, std::min(kCoopMaxBlocks, max_tokens));
+  const int64_t body = std::max(num_experts * hist_blocks, e_pad * coop_blocks) * 4;
+  const size_t bytes = kWsHeaderBytes + static_cast<size_t>(body);
   return (bytes + 255) / 256 * 256;
 }
 
 constexpr int kGatherV = 8;     // vectors per lane in one gather chunk
 constexpr int kFusedV = 4;      // same, inside the 1024-thread fused kernel
-constexpr int kUnpermuteV = 2;  // vectors per lane in one unpermute chunk
+constexpr int kCoopV = 4;       // same, inside the cooperative kernel
+constexpr int64_t kFusedMaxRows = 1024;  // R above this: the cooperative kernel
 
 // (token, chunk) work items of a row kernel.
 int64_t row_items(int64_t T, int64_t row_vecs, int V) {
@@ -159,6 +166,40 @@ cudaError_t launch_fused(const IdT* ids, const int32_t* emap, int64_t T, int K, 
                 scales, scale_cols, static_cast<VecT*>(out), out_scales, offsets, pidx, inv, hdr);
 }
 
+template <typename IdT, typename VecT, int V>
+cudaError_t launch_coop(const IdT* ids, const int32_t* emap, int64_t T, int K, int E, int E_local,
+                        const void* hidden, int64_t row_bytes, const float* scales,
+                        int64_t scale_cols, void* out, float* out_scales, int64_t* offsets,
+                        int32_t* pidx, int32_t* inv, WsHeader* hdr, const DeviceInfo* d,
+                        cudaStream_t s) {
+  auto kern = k_permute_coop<IdT, VecT, V>;
+  const size_t smem = (static_cast<size_t>(kCoopWarps) * E_local + 2 * E_local + 1) * sizeof(int);
+  cudaError_t err = allow_smem(kern, smem);
+  if (err != cudaSuccess) return err;
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCoopThreads, smem);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  int64_t B = std::min<int64_t>(T, static_cast<int64_t>(d->sm_count) * per_sm);
+  B = std::max<int64_t>(1, std::min(B, kCoopMaxBlocks));
+  int* table = reinterpret_cast<int*>(reinterpret_cast<char*>(hdr) + kWsHeaderBytes);
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(static_cast<unsigned>(B));
+  cfg.blockDim = dim3(kCoopThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // all blocks co-resident (grid barrier)
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int64_t row_vecs = row_bytes / static_cast<int64_t>(sizeof(VecT));
+  return cudaLaunchKernelEx(&cfg, kern, ids, emap, T, K, E, E_local,
+                            static_cast<const VecT*>(hidden), row_vecs, scales, scale_cols,
+                            static_cast<VecT*>(out), out_scales, offsets, pidx, inv, hdr, table);
+}
+
 template <typename VecT, int V>
 cudaError_t launch_gather(const void* hidden, int64_t row_bytes, const float* scales,
                           int64_t scale_cols, const int32_t* inv, int64_t T, int K, void* out,
@@ -180,7 +221,7 @@ cudaError_t permute_typed(const IdT* ids, const int32_t* emap, int64_t T, int K,
   WsHeader* hdr = static_cast<WsHeader*>(ws);
   const int64_t R = T * K;
   const size_t vb = out == nullptr ? 16 : vec_bytes(row_bytes, hidden, out);
-  if (R <= kMetaChunkRows) {
+  if (R <= kFusedMaxRows) {
     switch (vb) {
       case 16: return launch_fused<IdT, uint4, kFusedV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
       case 8: return launch_fused<IdT, uint2, kFusedV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
@@ -189,37 +230,38 @@ cudaError_t permute_typed(const IdT* ids, const int32_t* emap, int64_t T, int K,
       default: return launch_fused<IdT, uint8_t, kFusedV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
     }
   }
-  const unsigned B = static_cast<unsigned>(ceil_div(R, kMetaChunkRows));
-  int* hist = reinterpret_cast<int*>(static_cast<char*>(ws) + kWsHeaderBytes);
-  const size_t smem_hist = static_cast<size_t>(E_local) * sizeof(int);
-  const size_t smem_scatter = (static_cast<size_t>(kMetaWarps) + 1) * E_local * sizeof(int);
-  cudaError_t err = allow_smem(k_route_scatter<IdT>, smem_scatter);
-  if (err != cudaSuccess) return err;
-  err = launch(k_route_hist<IdT>, B, kMetaThreads, smem_hist, s, ids, emap, R, E, E_local, hist,
-               offsets, hdr);
-  if (err != cudaSuccess) return err;
-  err = launch(k_route_scatter<IdT>, B, kMetaThreads, smem_scatter, s, ids, emap, R, E, E_local,
-               static_cast<const int*>(hist), static_cast<const int64_t*>(offsets), pidx, inv);
-  if (err != cudaSuccess || out == nullptr) return err;
   switch (vb) {
-    case 16: return launch_gather<uint4, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, d, s);
-    case 8: return launch_gather<uint2, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, d, s);
-    case 4: return launch_gather<uint32_t, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, d, s);
-    case 2: return launch_gather<uint16_t, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, d, s);
-    default: return launch_gather<uint8_t, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, d, s);
+    case 16: return launch_coop<IdT, uint4, kCoopV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
+    case 8: return launch_coop<IdT, uint2, kCoopV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
+    case 4: return launch_coop<IdT, uint32_t, kCoopV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
+    case 2: return launch_coop<IdT, uint16_t, kCoopV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
+    default: return launch_coop<IdT, uint8_t, kCoopV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
   }
 }
 
+template <typename VecT, int KG, int V>
+cudaError_t launch_unpermute_kv(const void* rows, int64_t num_rows, int64_t H, const float* w,
+                                const int32_t* inv, int64_t T, int K, void* out,
+                                unsigned* status, const DeviceInfo* d, cudaStream_t s) {
+  const int64_t row_vecs = H * 2 / static_cast<int64_t>(sizeof(VecT));
+  auto kern = k_unpermute<VecT, KG, V>;
+  const unsigned grid = item_grid(row_items(T, row_vecs, V), kRowWarps, d,
+                                  blocks_per_sm(kern, kRowThreads, 0));
+  return launch(kern, grid, kRowThreads, 0, s, static_cast<const VecT*>(rows), num_rows, row_vecs,
+                w, inv, T, K, static_cast<VecT*>(out), status);
+}
+
+// Rows whose loads are in flight together (KG) times vectors per lane (V):
+// about 8 vectors per lane for any K.
 template <typename VecT>
 cudaError_t launch_unpermute(const void* rows, int64_t num_rows, int64_t H, const float* w,
                              const int32_t* inv, int64_t T, int K, void* out, unsigned* status,
                              const DeviceInfo* d, cudaStream_t s) {
-  const int64_t row_vecs = H * 2 / static_cast<int64_t>(sizeof(VecT));
-  auto kern = k_unpermute<VecT, kUnpermuteV>;
-  const unsigned grid = item_grid(row_items(T, row_vecs, kUnpermuteV), kRowWarps, d,
-                                  blocks_per_sm(kern, kRowThreads, 0));
-  return launch(kern, grid, kRowThreads, 0, s, static_cast<const VecT*>(rows), num_rows, row_vecs,
-                w, inv, T, K, static_cast<VecT*>(out), status);
+  if (K == 1)
+    return launch_unpermute_kv<VecT, 1, 8>(rows, num_rows, H, w, inv, T, K, out, status, d, s);
+  if (K == 2)
+    return launch_unpermute_kv<VecT, 2, 4>(rows, num_rows, H, w, inv, T, K, out, status, d, s);
+  return launch_unpermute_kv<VecT, 4, 2>(rows, num_rows, H, w, inv, T, K, out, status, d, s);
 }
 
 int elem_bytes(moe_dtype_t dt) {

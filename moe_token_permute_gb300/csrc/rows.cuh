@@ -220,17 +220,17 @@ struct Bf16Vec {
   };
 };
 
-constexpr int kUnpermuteGroup = 4;  // kept rows whose loads are in flight together
-
 // Unpermute: warp per (token, chunk).  k ascending, fp32 multiply then fp32
 // add per term (no contraction), one bf16 round-to-nearest-even at the end.
-template <typename VecT, int V>
+// The loads of up to KG kept rows are in flight together; KG * V is kept near
+// 8 vectors per lane whatever K is.
+template <typename VecT, int KG, int V>
 __global__ void __launch_bounds__(kRowThreads)
 k_unpermute(const VecT* __restrict__ rows, int64_t num_rows, int64_t row_vecs,
             const float* __restrict__ topk_weights, const int32_t* __restrict__ inv_permuted_idx,
             int64_t T, int K, VecT* __restrict__ out, unsigned* __restrict__ status) {
   constexpr int kE = Bf16Vec<VecT>::kElems;
-  constexpr int kG = kUnpermuteGroup;
+  constexpr int kG = KG;
   constexpr int64_t kChunk = 32 * V;
   pdl_wait();
   const int lane = threadIdx.x & 31;

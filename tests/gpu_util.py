@@ -25,7 +25,7 @@ def bits16(t: torch.Tensor) -> np.ndarray:
 def bytes_of(t: torch.Tensor) -> np.ndarray:
     """Any tensor -> its raw bytes [rows, row_bytes] on the host."""
     t = t.detach().cpu().contiguous()
-    row_bytes = t.element_size() * (t[0].numel() if t.dim() > 1 else 1)
+    row_bytes = t.element_size() * int(np.prod(t.shape[1:], dtype=np.int64))
     return t.view(torch.uint8).numpy().reshape(t.shape[0], row_bytes)
 
 
@@ -82,8 +82,7 @@ def assert_metadata_equal(bufs, ref):
 
 def assert_rows_equal_full(inp, bufs, ref_full):
     n = ref_full["n_valid"]
-    np.testing.assert_array_equal(bytes_of(bufs["ph"][:n]),
-                                  ref_full["permuted_hidden"][:n].reshape(n, -1))
+    np.testing.assert_array_equal(bytes_of(bufs["ph"][:n]), ref_full["permuted_hidden"][:n])
     if bufs["ps"] is not None:
         np.testing.assert_array_equal(bufs["ps"][:n].cpu().numpy(), ref_full["permuted_scales"][:n])
 

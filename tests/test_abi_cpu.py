@@ -55,8 +55,8 @@ def test_workspace_size(lib):
     a = ws(4096, 2, 8)
     c = ws(32768, 8, 256)
     assert a % 256 == 0 and c % 256 == 0
-    # 32768*8 rows = 32 chunks of 8192 rows; one int per (expert, chunk)
-    assert c == 256 + 256 * 32 * 4
+    # per-block histogram table: one int per (expert, block), up to 1024 blocks
+    assert c == 256 + 256 * 1024 * 4
     assert ws(100, 8, 256) <= c  # monotone in tokens
     assert ws(-1, 2, 8) == 0
     assert ws(16, 0, 8) == 0
