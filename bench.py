@@ -211,7 +211,15 @@ class Setup:
         self.mp.moe_unpermute(self.rows, self.w, self.inv, self.out, workspace=self.ws)
 
     def launches_per_permute(self):
-        return 1 if self.T * self.wl.K <= 8192 else 3
+        return 1
+
+    def footprint(self):
+        ts = [self.hidden, self.scales, self.ids, self.w, self.rows, self.emap, self.offsets,
+              self.pidx, self.inv, self.ph, self.ps, self.out]
+        return sum(t.numel() * t.element_size() for t in ts if t is not None)
+
+
+L2_BYTES = 129 * 1024 * 1024
 
 
 def timed_calls(fn, n, flush=None):
@@ -229,17 +237,33 @@ def timed_calls(fn, n, flush=None):
     return 1e3 * sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / n
 
 
-def graph_us(fn, n=100):
+def back_to_back_us(fns, n):
+    """Mean device time (us) per call of n back-to-back calls cycling through
+    fns (one per buffer set), one event pair around all of them."""
+    for f in fns:
+        f()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(n):
+        fns[i % len(fns)]()
+    b.record()
+    torch.cuda.synchronize()
+    return 1e3 * a.elapsed_time(b) / n
+
+
+def graph_us(fns, n=100):
     """Per-call time from replaying a CUDA graph of n back-to-back calls."""
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        fn()
+        for f in fns:
+            f()
     torch.cuda.current_stream().wait_stream(s)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        for _ in range(n):
-            fn()
+        for i in range(n):
+            fns[i % len(fns)]()
     g.replay()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -253,28 +277,38 @@ def graph_us(fn, n=100):
 
 
 def sweep(dev, peak, flush):
+    """Per (workload, T): permute and unpermute timed separately, rotating over
+    enough buffer sets that the footprint is at least 3x the L2 size (or 64
+    sets for the smallest batches).  *_us is the device time per call from
+    replaying a CUDA graph of back-to-back calls (no Python launch cost);
+    *_eager_us the same calls launched one by one from Python; at T = 1 also a
+    single eager call after an L2 flush."""
     rows = []
     for name, wl in WORKLOADS.items():
         if name == "tiny":
             continue
         for T in wl.T_sweep:
-            s = Setup(name, T, seed=0, dev=dev)
-            for _ in range(3):
-                s.permute()
-                s.unpermute()
-            n = 30 if T >= 4096 else 100
-            p_us = timed_calls(s.permute, n, flush)
-            u_us = timed_calls(s.unpermute, n, flush)
-            rec = {"workload": name, "T": T,
-                   "permute_us": round(p_us, 2), "permute_GBps": round(s.pbytes / p_us / 1e3, 1),
-                   "permute_frac": round(s.pbytes / p_us / 1e3 / peak, 4),
-                   "unpermute_us": round(u_us, 2), "unpermute_GBps": round(s.ubytes / u_us / 1e3, 1),
-                   "unpermute_frac": round(s.ubytes / u_us / 1e3 / peak, 4)}
+            first = Setup(name, T, seed=0, dev=dev)
+            fp = first.footprint()
+            n_sets = int(min(64, max(2, -(-3 * L2_BYTES // max(fp, 1)))))
+            sets = [first] + [Setup(name, T, seed=i, dev=dev) for i in range(1, n_sets)]
+            n = max(3 * n_sets, 30 if T >= 4096 else 200)
+            n_graph = max(n_sets, 20 if T >= 4096 else 100)
+            p_us = graph_us([s.permute for s in sets], n_graph)
+            u_us = graph_us([s.unpermute for s in sets], n_graph)
+            s0 = sets[0]
+            rec = {"workload": name, "T": T, "sets": n_sets,
+                   "permute_us": round(p_us, 2), "permute_GBps": round(s0.pbytes / p_us / 1e3, 1),
+                   "permute_frac": round(s0.pbytes / p_us / 1e3 / peak, 4),
+                   "unpermute_us": round(u_us, 2), "unpermute_GBps": round(s0.ubytes / u_us / 1e3, 1),
+                   "unpermute_frac": round(s0.ubytes / u_us / 1e3 / peak, 4),
+                   "permute_eager_us": round(back_to_back_us([s.permute for s in sets], n), 2),
+                   "unpermute_eager_us": round(back_to_back_us([s.unpermute for s in sets], n), 2)}
             if T == 1:
-                rec["permute_graph_us"] = round(graph_us(s.permute), 2)
-                rec["unpermute_graph_us"] = round(graph_us(s.unpermute), 2)
+                rec["permute_after_flush_us"] = round(timed_calls(s0.permute, 50, flush), 2)
+                rec["unpermute_after_flush_us"] = round(timed_calls(s0.unpermute, 50, flush), 2)
             rows.append(rec)
-            del s
+            del sets, first, s0
             torch.cuda.empty_cache()
     return rows
 

@@ -102,16 +102,16 @@ MOE_API const char *moe_status_string(int status);
  * with at most `max_tokens` tokens needs, for `topk` and `num_experts` (global
  * experts).  Returns 0 for invalid arguments (max_tokens < 0, topk < 1 or
  * > MOE_MAX_TOPK, num_experts < 1, or max_tokens*topk > INT32_MAX).
- * The workspace holds per-block expert histograms, a completion ticket and
- * the status word.  (Digest of vLLM PR #43014, "implementation breakdown"
+ * The workspace holds the per-block expert histograms of one call, the
+ * grid-barrier words and the status word.  (Digest of vLLM PR #43014, "implementation breakdown"
  * item 3: the sort workspace is sized by a query op and pre-allocated.)
  */
 MOE_API size_t moe_permute_workspace_size(int64_t max_tokens, int32_t topk,
                                   int32_t num_experts);
 
 /*
- * moe_permute_workspace_init: zero the workspace's control words (ticket and
- * status).  Call once after allocating the workspace (async on `stream`); every
+ * moe_permute_workspace_init: zero the workspace's control words (grid
+ * barrier and status).  Call once after allocating the workspace (async on `stream`); every
  * later call leaves the workspace ready for the next one.  `workspace` must be
  * 256-byte aligned and at least moe_permute_workspace_size(...) bytes.
  */

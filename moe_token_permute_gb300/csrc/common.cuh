@@ -14,7 +14,7 @@ constexpr unsigned kFullMask = 0xffffffffu;
 
 // Workspace control block: first 256 bytes of every workspace.
 struct WsHeader {
-  unsigned ticket;  // blocks of the histogram kernel that have finished
+  unsigned reserved0;
   unsigned status;  // OR of MOE_FLAG_* bits
   unsigned arrive;  // grid barrier: blocks arrived (the last one resets it)
   unsigned gen;     // grid barrier: generation, bumped once per barrier

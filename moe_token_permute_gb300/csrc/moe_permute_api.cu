@@ -7,10 +7,14 @@
 // workspace (same digest, "implementation breakdown" items 1-3).
 //
 // Dispatch:
-//   R = T*K <= kMetaChunkRows: one fused launch (k_permute_fused).
-//   otherwise: k_route_hist -> k_route_scatter -> k_gather_rows, chained with
-//   programmatic dependent launch so each grid's launch latency overlaps the
-//   previous grid's tail.
+//   R = T*K <= kFusedMaxRows: one launch of k_permute_fused; every block
+//     redundantly ranks all rows and the blocks share the row copy (no
+//     inter-block communication);
+//   otherwise: k_route_coop (cooperative grid, one grid barrier) writes the
+//     metadata, and k_gather_rows, launched as its programmatic dependent,
+//     loads rows while the routing runs and stores them once it has finished.
+// Every launch carries programmatic stream serialization, so its launch
+// latency overlaps the previous kernel's tail.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -22,7 +26,7 @@
 #include "common.cuh"
 #include "routing.cuh"
 #include "rows.cuh"
-#include "permute_coop.cuh"
+#include "route_coop.cuh"
 
 namespace moe {
 namespace {
@@ -102,19 +106,18 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 constexpr int64_t kCoopMaxBlocks = 1024;  // table rows reserved for the cooperative grid
 
+// Header plus the cooperative kernel's per-block histogram table
+// [min(max_tokens, kCoopMaxBlocks)][num_experts rounded up to 4].
 size_t workspace_bytes_for(int64_t max_tokens, int32_t topk, int32_t num_experts) {
-  const int64_t R = max_tokens * topk;
-  const int64_t hist_blocks = std::max<int64_t>(1, ceil_div(R, kMetaChunkRows));
-  const int64_t e_pad = (num_experts + 3) / 4 * 4;
-  const int64_t coop_blocks = std::max<int64_t>(1, std::min(kCoopMaxBlocks, max_tokens));
-  const int64_t body = std::max(num_experts * hist_blocks, e_pad * coop_blocks) * 4;
-  const size_t bytes = kWsHeaderBytes + static_cast<size_t>(body);
+  (void)topk;
+  const int64_t e_pad = (static_cast<int64_t>(num_experts) + 3) / 4 * 4;
+  const int64_t blocks = std::max<int64_t>(1, std::min(kCoopMaxBlocks, max_tokens));
+  const size_t bytes = kWsHeaderBytes + static_cast<size_t>(e_pad * blocks * 4);
   return (bytes + 255) / 256 * 256;
 }
 
-constexpr int kGatherV = 8;     // vectors per lane in one gather chunk
-constexpr int kFusedV = 4;      // same, inside the 1024-thread fused kernel
-constexpr int kCoopV = 4;       // same, inside the cooperative kernel
+constexpr int kFusedV = 4;   // vectors per lane in one gather chunk (fused kernel)
+constexpr int kGatherV = 8;  // same, gather kernel of the large-batch path
 constexpr int64_t kFusedMaxRows = 1024;  // R above this: the cooperative kernel
 
 // (token, chunk) work items of a row kernel.
@@ -159,57 +162,54 @@ cudaError_t launch_fused(const IdT* ids, const int32_t* emap, int64_t T, int K, 
   cudaError_t err = allow_smem(kern, smem);
   if (err != cudaSuccess) return err;
   const int64_t row_vecs = row_bytes / static_cast<int64_t>(sizeof(VecT));
-  const unsigned grid =
-      out == nullptr ? 1u : item_grid(row_items(T, row_vecs, V), kMetaWarps, d, 1);
+  // One block per SM at most (each block redoes the routing), at least one
+  // item per block.
+  const unsigned grid = out == nullptr ? 1u : item_grid(row_items(T, row_vecs, V), 1, d, 1);
   return launch(kern, grid, kMetaThreads, smem, s, ids, emap, T, K, E, E_local,
                 static_cast<const VecT*>(hidden), row_bytes / static_cast<int64_t>(sizeof(VecT)),
                 scales, scale_cols, static_cast<VecT*>(out), out_scales, offsets, pidx, inv, hdr);
 }
 
-template <typename IdT, typename VecT, int V>
-cudaError_t launch_coop(const IdT* ids, const int32_t* emap, int64_t T, int K, int E, int E_local,
-                        const void* hidden, int64_t row_bytes, const float* scales,
-                        int64_t scale_cols, void* out, float* out_scales, int64_t* offsets,
-                        int32_t* pidx, int32_t* inv, WsHeader* hdr, const DeviceInfo* d,
-                        cudaStream_t s) {
-  auto kern = k_permute_coop<IdT, VecT, V>;
-  const size_t smem = (static_cast<size_t>(kCoopWarps) * E_local + 2 * E_local + 1) * sizeof(int);
+template <typename IdT>
+cudaError_t launch_route(const IdT* ids, const int32_t* emap, int64_t T, int K, int E, int E_local,
+                         int64_t* offsets, int32_t* pidx, int32_t* inv, WsHeader* hdr,
+                         const DeviceInfo* d, cudaStream_t s) {
+  auto kern = k_route_coop<IdT>;
+  const size_t smem = (static_cast<size_t>(kRouteWarps) * E_local + 2 * E_local + 1) * sizeof(int);
   cudaError_t err = allow_smem(kern, smem);
   if (err != cudaSuccess) return err;
-  int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCoopThreads, smem);
-  if (err != cudaSuccess) return err;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  int64_t B = std::min<int64_t>(T, static_cast<int64_t>(d->sm_count) * per_sm);
+  // One routing block per SM: the rest of each SM stays free for the gather
+  // blocks that start while routing runs.
+  int64_t B = std::min<int64_t>(T, d->sm_count);
   B = std::max<int64_t>(1, std::min(B, kCoopMaxBlocks));
   int* table = reinterpret_cast<int*>(reinterpret_cast<char*>(hdr) + kWsHeaderBytes);
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3(static_cast<unsigned>(B));
-  cfg.blockDim = dim3(kCoopThreads);
+  cfg.blockDim = dim3(kRouteThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;  // all blocks co-resident (grid barrier)
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const int64_t row_vecs = row_bytes / static_cast<int64_t>(sizeof(VecT));
-  return cudaLaunchKernelEx(&cfg, kern, ids, emap, T, K, E, E_local,
-                            static_cast<const VecT*>(hidden), row_vecs, scales, scale_cols,
-                            static_cast<VecT*>(out), out_scales, offsets, pidx, inv, hdr, table);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, ids, emap, T, K, E, E_local, offsets, pidx, inv, hdr,
+                            table);
 }
 
 template <typename VecT, int V>
 cudaError_t launch_gather(const void* hidden, int64_t row_bytes, const float* scales,
                           int64_t scale_cols, const int32_t* inv, int64_t T, int K, void* out,
-                          float* out_scales, const DeviceInfo* d, cudaStream_t s) {
+                          float* out_scales, cudaStream_t s) {
   const int64_t row_vecs = row_bytes / static_cast<int64_t>(sizeof(VecT));
-  auto kern = k_gather_rows<VecT, V>;
-  const unsigned grid = item_grid(row_items(T, row_vecs, V), kRowWarps, d,
-                                  blocks_per_sm(kern, kRowThreads, 0));
-  return launch(kern, grid, kRowThreads, 0, s, static_cast<const VecT*>(hidden), row_vecs, scales,
-                scale_cols, inv, T, K, static_cast<VecT*>(out), out_scales);
+  const int64_t blocks = ceil_div(row_items(T, row_vecs, V), kRowWarps);
+  if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
+  return launch(k_gather_rows<VecT, V>, static_cast<unsigned>(blocks), kRowThreads, 0, s,
+                static_cast<const VecT*>(hidden), row_vecs, scales, scale_cols, inv, T, K,
+                static_cast<VecT*>(out), out_scales);
 }
 
 template <typename IdT>
@@ -230,12 +230,14 @@ cudaError_t permute_typed(const IdT* ids, const int32_t* emap, int64_t T, int K,
       default: return launch_fused<IdT, uint8_t, kFusedV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
     }
   }
+  cudaError_t err = launch_route<IdT>(ids, emap, T, K, E, E_local, offsets, pidx, inv, hdr, d, s);
+  if (err != cudaSuccess || out == nullptr) return err;
   switch (vb) {
-    case 16: return launch_coop<IdT, uint4, kCoopV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
-    case 8: return launch_coop<IdT, uint2, kCoopV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
-    case 4: return launch_coop<IdT, uint32_t, kCoopV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
-    case 2: return launch_coop<IdT, uint16_t, kCoopV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
-    default: return launch_coop<IdT, uint8_t, kCoopV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
+    case 16: return launch_gather<uint4, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, s);
+    case 8: return launch_gather<uint2, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, s);
+    case 4: return launch_gather<uint32_t, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, s);
+    case 2: return launch_gather<uint16_t, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, s);
+    default: return launch_gather<uint8_t, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, s);
   }
 }
 

@@ -1,20 +1,14 @@
-// routing.cuh -- routing metadata of moe_permute as a stable counting sort.
+// routing.cuh -- device helpers of the stable counting sort behind moe_permute.
 //
 // vLLM PR #14568 ("permute/unpermute kernel for moe optimization",
 // description): permute orders the expanded rows r = t*K + k by expert so each
 // expert's rows are contiguous for the grouped GEMM.  The prior art sorts with
 // a generic radix sort and a sort workspace (vLLM PR #43014 digest,
 // "implementation breakdown" item 3).  Here the key range is only the number
-// of local experts, so the sort is a counting sort:
-//   k_route_hist     per-block expert histogram (warp-aggregated shared
-//                    atomics); the last block to finish scans all histograms
-//                    into per-(expert, block) bases and writes
-//                    expert_first_token_offset.
-//   k_route_scatter  per-block stable ranks (match_any peer groups inside a
-//                    warp, per-warp counts scanned across warps), then
-//                    p = base[e][b] + rank; writes permuted_idx / inv_permuted_idx.
-// Chunks: block b owns rows [b*C, (b+1)*C), C = kMetaWarps * 32 * kMetaRowsPerLane;
-// warp w of a block owns the contiguous rows [w*32*J, (w+1)*32*J) of the chunk,
+// of local experts, so the sort is a counting sort: a per-expert histogram,
+// an exclusive scan of the counts, and a stable scatter whose ranks come from
+// match_any peer groups inside a warp plus per-warp counts scanned across the
+// warps of a block.  Warp w of a block owns a contiguous slice of 32*J rows,
 // so ranks computed warp by warp in row order are stable.
 #pragma once
 
@@ -25,7 +19,7 @@ namespace moe {
 constexpr int kMetaThreads = 1024;
 constexpr int kMetaWarps = kMetaThreads / kWarpSize;
 constexpr int kMetaRowsPerLane = 8;  // J
-constexpr int kMetaChunkRows = kMetaThreads * kMetaRowsPerLane;  // C = 8192
+constexpr int kMetaChunkRows = kMetaThreads * kMetaRowsPerLane;  // rows one block ranks: 8192
 
 // Local expert of one global id, or -1 when the row is dropped.
 template <typename IdT>
@@ -100,130 +94,6 @@ __device__ __forceinline__ void scan_counts_over_warps(int* cnt, int E_local, in
     }
     s_total[e] = run;
   }
-}
-
-// Kernel 1: per-block histogram; the last block scans every histogram.
-// hist: [E_local][B] ints in the workspace; on exit (last block) it holds the
-// exclusive prefix over (e-major, b-minor) order, i.e. the first output
-// position of expert e's rows from block b.
-template <typename IdT>
-__global__ void __launch_bounds__(kMetaThreads)
-k_route_hist(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
-             int64_t R, int E, int E_local, int* __restrict__ hist,
-             int64_t* __restrict__ offsets, WsHeader* __restrict__ hdr) {
-  extern __shared__ int s_hist[];  // [E_local]
-  __shared__ int s_warp[32];
-  __shared__ int s_is_last;
-  pdl_wait();
-  pdl_launch_dependents();
-
-  const int B = gridDim.x;
-  const int b = blockIdx.x;
-  const int lane = threadIdx.x & 31;
-  for (int e = threadIdx.x; e < E_local; e += blockDim.x) s_hist[e] = 0;
-  __syncthreads();
-
-  const int64_t chunk0 = static_cast<int64_t>(b) * kMetaChunkRows;
-  const int64_t row_end = min(R, chunk0 + kMetaChunkRows);
-  const int64_t slice0 = chunk0 + static_cast<int64_t>(threadIdx.x >> 5) * 32 * kMetaRowsPerLane;
-  int key[kMetaRowsPerLane];
-  unsigned flags = 0;
-  load_keys<IdT, kMetaRowsPerLane>(ids, emap, E, E_local, slice0, row_end, key, flags);
-#pragma unroll
-  for (int j = 0; j < kMetaRowsPerLane; ++j) {
-    const int e = key[j];
-    const unsigned peers = __match_any_sync(kFullMask, e);
-    if (e >= 0 && (peers & lanemask_lt()) == 0) atomicAdd(&s_hist[e], __popc(peers));
-  }
-  flags = __reduce_or_sync(kFullMask, flags);
-  if (flags != 0 && lane == 0) atomicOr(&hdr->status, flags);
-  __syncthreads();
-  for (int e = threadIdx.x; e < E_local; e += blockDim.x)
-    hist[static_cast<int64_t>(e) * B + b] = s_hist[e];
-
-  // Last block to finish does the scan (no block ever waits for another).
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_is_last = atomicAdd(&hdr->ticket, 1u) == static_cast<unsigned>(B - 1);
-  __syncthreads();
-  if (!s_is_last) return;
-  __threadfence();
-
-  const int64_t n = static_cast<int64_t>(E_local) * B;
-  const int64_t seg = (n + blockDim.x - 1) / blockDim.x;
-  const int64_t i0 = min(n, static_cast<int64_t>(threadIdx.x) * seg);
-  const int64_t i1 = min(n, i0 + seg);
-  int sum = 0;
-#pragma unroll 8
-  for (int64_t i = i0; i < i1; ++i) sum += __ldcg(hist + i);
-  int total;
-  int run = block_exclusive_sum(sum, s_warp, &total);
-  for (int64_t i = i0; i < i1; ++i) {
-    const int c = __ldcg(hist + i);
-    hist[i] = run;
-    if (i % B == 0) offsets[i / B] = run;
-    run += c;
-  }
-  if (threadIdx.x == 0) {
-    offsets[E_local] = total;
-    hdr->ticket = 0u;  // ready for the next call on this workspace
-  }
-}
-
-// Kernel 2: stable scatter of the indices.  Ranks are computed before waiting
-// on kernel 1 (they depend only on the caller's ids), then combined with the
-// bases kernel 1 produced.
-template <typename IdT>
-__global__ void __launch_bounds__(kMetaThreads)
-k_route_scatter(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
-                int64_t R, int E, int E_local, const int* __restrict__ base,
-                const int64_t* __restrict__ offsets, int32_t* __restrict__ permuted_idx,
-                int32_t* __restrict__ inv_permuted_idx) {
-  extern __shared__ int smem[];  // cnt [kMetaWarps][E_local], s_base [E_local]
-  int* cnt = smem;
-  int* s_base = smem + kMetaWarps * E_local;
-  const int B = gridDim.x;
-  const int b = blockIdx.x;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < kMetaWarps * E_local; i += blockDim.x) cnt[i] = 0;
-  __syncthreads();
-
-  const int64_t chunk0 = static_cast<int64_t>(b) * kMetaChunkRows;
-  const int64_t row_end = min(R, chunk0 + kMetaChunkRows);
-  const int64_t slice0 = chunk0 + static_cast<int64_t>(warp) * 32 * kMetaRowsPerLane;
-  int key[kMetaRowsPerLane], rank[kMetaRowsPerLane];
-  unsigned flags = 0;  // already reported by kernel 1
-  load_keys<IdT, kMetaRowsPerLane>(ids, emap, E, E_local, slice0, row_end, key, flags);
-  rank_warp_slice<kMetaRowsPerLane>(key, cnt + warp * E_local, rank);
-  __syncthreads();
-  scan_counts_over_warps(cnt, E_local, kMetaWarps, s_base);  // s_base: scratch for totals
-
-  pdl_wait();  // kernel 1's bases and offsets are visible from here on
-  pdl_launch_dependents();
-  __syncthreads();
-  for (int e = threadIdx.x; e < E_local; e += blockDim.x)
-    s_base[e] = __ldcg(base + static_cast<int64_t>(e) * B + b);
-  __syncthreads();
-
-#pragma unroll
-  for (int j = 0; j < kMetaRowsPerLane; ++j) {
-    const int64_t r = slice0 + j * 32 + lane;
-    if (r < row_end) {
-      const int e = key[j];
-      int p = -1;
-      if (e >= 0) {
-        p = s_base[e] + cnt[warp * E_local + e] + rank[j];
-        permuted_idx[p] = static_cast<int32_t>(r);
-      }
-      inv_permuted_idx[r] = p;
-    }
-  }
-  // Tail of permuted_idx: positions [N_valid, R) hold -1.
-  const int64_t n_valid = __ldcg(offsets + E_local);
-  for (int64_t p = n_valid + static_cast<int64_t>(b) * blockDim.x + threadIdx.x; p < R;
-       p += static_cast<int64_t>(B) * blockDim.x)
-    permuted_idx[p] = -1;
 }
 
 }  // namespace moe

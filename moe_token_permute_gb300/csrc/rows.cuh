@@ -73,11 +73,12 @@ __device__ __forceinline__ void copy_token_scales(const float* __restrict__ src,
   }
 }
 
-// Kernel 3: row gather driven by inv_permuted_idx (written by kernel 2).
-// The grid starts once the routing kernels have passed their own dependency
-// waits, so the caller's hidden rows are complete: each warp loads its first
-// chunk before waiting for the index maps, overlapping that load with the tail
-// of the routing kernels.
+// Row gather of the large-batch permute: one warp per (token, chunk) item, one
+// item per warp, so the hardware block scheduler balances the work across SMs.
+// Launched as the dependent of the routing grid, which lets it start early:
+// the caller's hidden rows are complete by then (the routing grid has passed
+// its own dependency wait), so each warp loads its chunk first and only then
+// waits for the routing grid before reading inv_permuted_idx.
 template <typename VecT, int V>
 __global__ void __launch_bounds__(kRowThreads)
 k_gather_rows(const VecT* __restrict__ hidden, int64_t row_vecs,
@@ -87,35 +88,25 @@ k_gather_rows(const VecT* __restrict__ hidden, int64_t row_vecs,
   constexpr int64_t kChunk = 32 * V;
   const int lane = threadIdx.x & 31;
   const int64_t n_chunks = (row_vecs + kChunk - 1) / kChunk;
-  const int64_t n_items = T * n_chunks;
-  const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (item >= T * n_chunks) return;
+  const int64_t t = item / n_chunks;
+  const int64_t c0 = (item - t * n_chunks) * kChunk;
   VecT v[V];
-  bool have = false;
-  if (warp0 < n_items) {
-    const int64_t t = warp0 / n_chunks;
-    load_chunk<VecT, V>(hidden + t * row_vecs, (warp0 - t * n_chunks) * kChunk, row_vecs, v);
-    have = true;
-  }
+  load_chunk<VecT, V>(hidden + t * row_vecs, c0, row_vecs, v);
   pdl_wait();
-  for (int64_t item = warp0; item < n_items; item += n_warps) {
-    const int64_t t = item / n_chunks;
-    const int64_t c0 = (item - t * n_chunks) * kChunk;
-    const int p = lane < K ? __ldcg(inv_permuted_idx + t * K + lane) : -1;
-    const unsigned valid = __ballot_sync(kFullMask, p >= 0);
-    if (valid == 0u) {  // every row of this token was dropped
-      have = false;
-      continue;
-    }
-    if (!have) load_chunk<VecT, V>(hidden + t * row_vecs, c0, row_vecs, v);
-    have = false;
-    store_chunk<VecT, V>(v, permuted_hidden, c0, row_vecs, p, valid);
-    if (permuted_scales != nullptr && c0 == 0)
-      copy_token_scales(scales + t * scale_cols, scale_cols, permuted_scales, p, valid);
-  }
+  int p = lane < K ? __ldcg(inv_permuted_idx + t * K + lane) : -1;
+  // Positions outside [0, T*K) can only come from a routing grid that gave up
+  // (status MOE_FLAG_BARRIER_TIMEOUT); never store through them.
+  if (p >= T * K) p = -1;
+  const unsigned valid = __ballot_sync(kFullMask, p >= 0);
+  if (valid == 0u) return;  // every row of this token was dropped
+  store_chunk<VecT, V>(v, permuted_hidden, c0, row_vecs, p, valid);
+  if (permuted_scales != nullptr && c0 == 0)
+    copy_token_scales(scales + t * scale_cols, scale_cols, permuted_scales, p, valid);
 }
 
-// Single-launch permute for R <= kMetaChunkRows expanded rows.  Every block
+// Single-launch permute for small batches (R <= kMetaChunkRows expanded rows).  Every block
 // computes the whole stable counting sort in shared memory (R is small, the
 // ids come from L2), block 0 writes the metadata, and all blocks share the
 // row copy: no block ever waits for another.
@@ -191,12 +182,13 @@ k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
   if (permuted_hidden == nullptr) return;
   __syncthreads();
 
+  // Items go round-robin over the blocks first (item i -> block i % G), so a
+  // small batch still spreads its copy over every block's SM.
   constexpr int64_t kChunk = 32 * V;
   const int64_t n_chunks = (row_vecs + kChunk - 1) / kChunk;
   const int64_t n_items = T * n_chunks;
-  const int64_t n_warps = static_cast<int64_t>(gridDim.x) * kMetaWarps;
-  for (int64_t item = static_cast<int64_t>(blockIdx.x) * kMetaWarps + warp; item < n_items;
-       item += n_warps) {
+  const int64_t G = gridDim.x;
+  for (int64_t item = blockIdx.x + warp * G; item < n_items; item += kMetaWarps * G) {
     const int64_t t = item / n_chunks;
     const int64_t c0 = (item - t * n_chunks) * kChunk;
     const int p = lane < K ? s_p[t * K + lane] : -1;

@@ -51,7 +51,7 @@ def test_library_built_for_sm103a_only():
 
 def test_workspace_size(lib):
     ws = lib.moe_permute_workspace_size
-    assert ws(0, 1, 1) == 256 + 256  # header + one (padded) histogram block
+    assert ws(0, 1, 1) == 256 + 256  # header + one (padded) histogram row
     a = ws(4096, 2, 8)
     c = ws(32768, 8, 256)
     assert a % 256 == 0 and c % 256 == 0
