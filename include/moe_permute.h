@@ -198,6 +198,46 @@ MOE_API int moe_read_status(const void *workspace, uint32_t *host_status,
 /* moe_clear_status: zero the status word (async on `stream`). */
 MOE_API int moe_clear_status(void *workspace, moe_stream_t stream);
 
+/*
+ * moe_permute_noalloc: moe_permute for callers that cannot allocate device
+ * memory at all, not even the small workspace moe_permute asks for.  Examples:
+ * a plugin whose host framework owns every device allocation and only hands
+ * over input and output pointers; a serving loop that must not call
+ * cudaMalloc once it is running, because cudaMalloc can synchronise the
+ * device and grow the memory footprint after start-up.  The pages have no
+ * counterpart of this entry point: their scratch buffers are always
+ * allocated by the caller.
+ *
+ * Arguments and results are exactly those of moe_permute without the
+ * workspace.  The scratch lives instead in one static device array of
+ * MOE_NOALLOC_SCRATCH_BYTES inside this library: every GPU that loads the
+ * library holds it until the process exits.  Nothing is allocated or freed.
+ *  - The first call on a device looks up that array's device address and
+ *    zeroes its control words (stream-ordered on `stream`).  Make that first
+ *    call before capturing any stream into a CUDA graph.
+ *  - Every call on a device shares the one array, which keeps the last call's
+ *    contents.  Calls that may overlap on the GPU (two streams, or parallel
+ *    graph branches) race on it; serialise them.
+ *  - A call whose scratch need, moe_permute_workspace_size(num_tokens, topk,
+ *    num_experts), exceeds MOE_NOALLOC_SCRATCH_BYTES returns
+ *    MOE_ERR_WORKSPACE_TOO_SMALL and enqueues nothing: up to 256 experts fit
+ *    for any token count, 512 experts up to 512 tokens, 1024 up to 256.
+ *  - Device status flags (MOE_FLAG_*) are kept in the shared array and are
+ *    not readable through this entry point; rows with bad ids are still
+ *    dropped exactly as moe_permute drops them.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES ((size_t)(1u << 20) + 256u)
+MOE_API int moe_permute_noalloc(const void *hidden_states, moe_dtype_t hidden_dtype,
+                                const float *hidden_scales, int64_t scale_cols,
+                                const void *topk_ids, moe_index_t topk_ids_dtype,
+                                const int32_t *expert_map,
+                                int64_t num_tokens, int64_t hidden_size, int32_t topk,
+                                int32_t num_experts, int32_t num_local_experts,
+                                void *permuted_hidden_states, float *permuted_scales,
+                                int64_t *expert_first_token_offset,
+                                int32_t *permuted_idx, int32_t *inv_permuted_idx,
+                                moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -437,3 +437,54 @@ int moe_clear_status(void* workspace, moe_stream_t stream) {
 }
 
 }  // extern "C"
+
+// ---- allocation-free variant of moe_permute ------------------------------
+// The scratch of moe_permute_noalloc: a file-scope device array, one per GPU
+// that loads this library.  Host code must never use its name as an address
+// (on the host it names a stand-in, not device memory): the device address
+// is looked up once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {nullptr};
+}  // namespace
+
+extern "C" int moe_permute_noalloc(const void* hidden_states, moe_dtype_t hidden_dtype,
+                                   const float* hidden_scales, int64_t scale_cols,
+                                   const void* topk_ids, moe_index_t topk_ids_dtype,
+                                   const int32_t* expert_map, int64_t num_tokens,
+                                   int64_t hidden_size, int32_t topk, int32_t num_experts,
+                                   int32_t num_local_experts, void* permuted_hidden_states,
+                                   float* permuted_scales, int64_t* expert_first_token_offset,
+                                   int32_t* permuted_idx, int32_t* inv_permuted_idx,
+                                   moe_stream_t stream) {
+  if (num_tokens >= 0 && topk >= 1 && topk <= MOE_MAX_TOPK && num_experts >= 1 &&
+      num_tokens <= INT32_MAX / topk &&
+      workspace_bytes_for(num_tokens, topk, num_experts) > MOE_NOALLOC_SCRATCH_BYTES)
+    return MOE_ERR_WORKSPACE_TOO_SMALL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev] == nullptr) {
+      // set-up, once per device, with that device current
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+        cudaGetLastError();
+        return MOE_ERR_CUDA;
+      }
+      if (cudaMemsetAsync(ptr, 0, kWsHeaderBytes, reinterpret_cast<cudaStream_t>(stream)) !=
+          cudaSuccess)
+        return MOE_ERR_CUDA;
+      g_noalloc_ptr[dev] = ptr;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  return moe_permute(hidden_states, hidden_dtype, hidden_scales, scale_cols, topk_ids,
+                     topk_ids_dtype, expert_map, num_tokens, hidden_size, topk, num_experts,
+                     num_local_experts, permuted_hidden_states, permuted_scales,
+                     expert_first_token_offset, permuted_idx, inv_permuted_idx, scratch,
+                     MOE_NOALLOC_SCRATCH_BYTES, stream);
+}

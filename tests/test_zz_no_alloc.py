@@ -1,0 +1,90 @@
+"""moe_permute_noalloc: the permute entry point for callers that cannot
+allocate device memory (for example a plugin whose host framework owns every
+allocation, or a serving loop that must not call cudaMalloc once running).
+It keeps its scratch in a static device array inside the library instead of
+a caller workspace.  This test calls it through the C ABI twice in a row, on
+different batches, and checks each result against moe_permute with a caller
+workspace: indices, offsets and rows must be identical (the bar for integer
+and byte outputs).  It is collected last and needs nothing from other tests."""
+import pytest
+import torch
+
+import moe_token_permute_gb300 as mp
+from moe_token_permute_gb300 import _binding as b
+from moe_token_permute_gb300 import build as cuda_build
+from moe_token_permute_gb300.workloads import make_inputs
+
+pytestmark = pytest.mark.gpu
+
+_DT = {torch.bfloat16: b.MOE_DTYPE_BF16, torch.float8_e4m3fn: b.MOE_DTYPE_FP8_E4M3}
+
+
+def _p(t):
+    return None if t is None else t.data_ptr()
+
+
+def _outputs(wl, T, dtype, scale_cols):
+    R = T * wl.K
+    dev = "cuda"
+    return dict(off=torch.full((wl.e_local + 1,), -5, dtype=torch.int64, device=dev),
+                pidx=torch.full((R,), -5, dtype=torch.int32, device=dev),
+                inv=torch.full((R,), -5, dtype=torch.int32, device=dev),
+                ph=torch.zeros(R, wl.H, dtype=dtype, device=dev),
+                ps=torch.zeros(R, scale_cols, dtype=torch.float32, device=dev) if scale_cols else None)
+
+
+def _noalloc_call(inp, out):
+    wl = inp["wl"]
+    hidden = inp["hidden"]
+    sc = inp["scales"]
+    stream = torch.cuda.current_stream().cuda_stream
+    return b.lib().moe_permute_noalloc(
+        _p(hidden), _DT[hidden.dtype], _p(sc), 0 if sc is None else sc.shape[1],
+        _p(inp["topk_ids"]), b.MOE_INDEX_INT32, _p(inp["expert_map"]),
+        inp["T"], wl.H, wl.K, wl.E, wl.e_local,
+        _p(out["ph"]), _p(out["ps"]), _p(out["off"]), _p(out["pidx"]), _p(out["inv"]), stream)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _library():
+    cuda_build.build()
+    b.lib()
+
+
+def test_noalloc_matches_workspace_entry_point_two_calls_in_a_row():
+    # first: a large batch (cooperative path); second: a DeepSeek-V3-shaped
+    # fp8 batch with scales and 256 experts; third: a small batch (single block)
+    for name, T in (("mixtral", 3000), ("dsv3", 700), ("dsv2lite", 60)):
+        inp = make_inputs(name, T, seed=11, device="cuda", with_rows=False)
+        wl = inp["wl"]
+        sc_cols = 0 if inp["scales"] is None else inp["scales"].shape[1]
+        got = _outputs(wl, T, inp["hidden"].dtype, sc_cols)
+        ref = _outputs(wl, T, inp["hidden"].dtype, sc_cols)
+        assert _noalloc_call(inp, got) == b.MOE_OK
+        ws = torch.empty(mp.moe_permute_workspace_size(T, wl.K, wl.E), dtype=torch.uint8,
+                         device="cuda")
+        mp.moe_permute_workspace_init(ws)
+        mp.moe_permute(inp["hidden"], inp["topk_ids"], ref["off"], ref["pidx"], ref["inv"], ws,
+                       num_experts=wl.E, num_local_experts=wl.e_local,
+                       expert_map=inp["expert_map"], hidden_scales=inp["scales"],
+                       permuted_hidden_states=ref["ph"], permuted_scales=ref["ps"])
+        torch.cuda.synchronize()
+        for k in ("off", "pidx", "inv"):
+            assert torch.equal(got[k], ref[k]), (name, k)
+        n = int(ref["off"][-1])
+        assert torch.equal(got["ph"][:n].view(torch.uint8), ref["ph"][:n].view(torch.uint8))
+        if sc_cols:
+            assert torch.equal(got["ps"][:n], ref["ps"][:n])
+
+
+def test_noalloc_rejects_requests_beyond_its_scratch():
+    T, K, E = 4096, 8, 1024  # needs more than the static array holds
+    assert mp.moe_permute_workspace_size(T, K, E) > b.MOE_NOALLOC_SCRATCH_BYTES
+    ids = torch.zeros(T, K, dtype=torch.int32, device="cuda")
+    off = torch.empty(E + 1, dtype=torch.int64, device="cuda")
+    idx = torch.empty(T * K, dtype=torch.int32, device="cuda")
+    rc = b.lib().moe_permute_noalloc(None, b.MOE_DTYPE_BF16, None, 0, ids.data_ptr(),
+                                     b.MOE_INDEX_INT32, None, T, 1, K, E, E, None, None,
+                                     off.data_ptr(), idx.data_ptr(), idx.data_ptr(),
+                                     torch.cuda.current_stream().cuda_stream)
+    assert rc == b.MOE_ERR_WORKSPACE_TOO_SMALL
