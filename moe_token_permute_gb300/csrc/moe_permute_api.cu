@@ -175,12 +175,15 @@ cudaError_t launch_route(const IdT* ids, const int32_t* emap, int64_t T, int K, 
                          int64_t* offsets, int32_t* pidx, int32_t* inv, WsHeader* hdr,
                          const DeviceInfo* d, cudaStream_t s) {
   auto kern = k_route_coop<IdT>;
-  const size_t smem = (static_cast<size_t>(kRouteWarps) * E_local + 2 * E_local + 1) * sizeof(int);
+  const size_t smem = (static_cast<size_t>(kRouteWarps) * E_local + 4 * E_local + 1) * sizeof(int);
   cudaError_t err = allow_smem(kern, smem);
   if (err != cudaSuccess) return err;
-  // One routing block per SM: the rest of each SM stays free for the gather
-  // blocks that start while routing runs.
-  int64_t B = std::min<int64_t>(T, d->sm_count);
+  // As few blocks as give each block at most one round of rows (so the ranks
+  // stay in registers), and at most one per SM: the histogram table every
+  // block reads after the barrier is [B][E], and the rest of each SM stays
+  // free for the gather blocks that start while routing runs.
+  const int64_t tokens_per_round = std::max<int64_t>(1, kRouteRoundRows / K);
+  int64_t B = std::min<int64_t>(ceil_div(T, tokens_per_round), d->sm_count);
   B = std::max<int64_t>(1, std::min(B, kCoopMaxBlocks));
   int* table = reinterpret_cast<int*>(reinterpret_cast<char*>(hdr) + kWsHeaderBytes);
   cudaLaunchConfig_t cfg;

@@ -21,7 +21,8 @@
 // starts: those blocks load their source rows while routing runs and wait for
 // this grid before they read inv_permuted_idx.
 // The barrier wait is bounded (2^24 polls or 2 s): on timeout the status word
-// gets MOE_FLAG_BARRIER_TIMEOUT and the kernel returns (outputs undefined).
+// gets MOE_FLAG_BARRIER_TIMEOUT and the kernel returns (outputs undefined; the
+// gather that follows never stores through an out-of-range position).
 #pragma once
 
 #include "common.cuh"
@@ -43,20 +44,24 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 
 // Grid-wide barrier for a cooperatively launched grid.  hdr->arrive counts
-// arrivals (the last one resets it), hdr->gen is bumped once per barrier.
-// Returns false (and flags the status word) if the wait gave up.
-__device__ __forceinline__ bool grid_barrier(WsHeader* hdr) {
+// arrivals (the last one resets it); hdr->gen is bumped once per barrier.
+// `gen` is the generation thread 0 read at kernel start: it cannot move before
+// every block of this grid has arrived.  Ordering: bar.sync gathers the
+// block's writes into thread 0, whose arrival is an acquire-release atomic;
+// the last block publishes with a release add on gen; waiters read gen with
+// acquire loads.  Returns false (and flags the status word) if the wait gave
+// up.
+__device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned gen) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    const unsigned gen = *reinterpret_cast<volatile unsigned*>(&hdr->gen);
-    __threadfence();
-    const unsigned arrived = atomicAdd(&hdr->arrive, 1u);
+    unsigned arrived;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                 : "=r"(arrived) : "l"(&hdr->arrive) : "memory");
     if (arrived == gridDim.x - 1) {
-      hdr->arrive = 0u;
-      __threadfence();
-      atomicAdd(&hdr->gen, 1u);
+      asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" :: "l"(&hdr->arrive) : "memory");
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(&hdr->gen) : "memory");
     } else {
       unsigned spins = 0;
       const unsigned long long t_start = global_ns();
@@ -70,19 +75,19 @@ __device__ __forceinline__ bool grid_barrier(WsHeader* hdr) {
           ok = 0;
           break;
         }
-        __nanosleep(32);
+        if (spins > 4096u) __nanosleep(64);
       }
     }
-    __threadfence();
     s_ok = ok;
   }
   __syncthreads();
   return s_ok != 0;
 }
 
-// Shared memory: s_base [E_local + 1] | s_run [E_local] | cnt [kRouteWarps][E_local]
+// Shared memory: s_base [E_local + 1] | s_run [E_local] | s_tot [E_local] |
+//                s_bef [E_local] | cnt [kRouteWarps][E_local]
 template <typename IdT>
-__global__ void __launch_bounds__(kRouteThreads)
+__global__ void __launch_bounds__(kRouteThreads, 4)
 k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
              int64_t T, int K, int E, int E_local,
              int64_t* __restrict__ offsets, int32_t* __restrict__ permuted_idx,
@@ -92,7 +97,10 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
   __shared__ int s_warp[32];
   int* s_base = smem;                 // [E_local + 1]
   int* s_run = s_base + E_local + 1;  // [E_local]
-  int* cnt = s_run + E_local;         // [kRouteWarps][E_local]
+  int* s_tot = s_run + E_local;       // [E_local] all blocks' rows per expert
+  int* s_bef = s_tot + E_local;       // [E_local] rows per expert in blocks before b
+  int* cnt = s_bef + E_local;         // [kRouteWarps][E_local]
+  __shared__ unsigned s_gen;
   const int B = gridDim.x;
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5;
@@ -107,6 +115,15 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
 
   pdl_wait();
   pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    unsigned g;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(&hdr->gen) : "memory");
+    s_gen = g;
+  }
+  for (int e = threadIdx.x; e < E_local; e += blockDim.x) {
+    s_tot[e] = 0;
+    s_bef[e] = 0;
+  }
 
   // Phase 1: histogram (and, for one round, the ranks).
   int key[J], rank[J];
@@ -137,16 +154,11 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
     table[static_cast<int64_t>(b) * e_pad + e] = e < E_local ? s_run[e] : 0;
 
   // Phase 2: every block's histogram is in the table after this.
-  if (!grid_barrier(hdr)) return;
+  if (!grid_barrier(hdr, s_gen)) return;
 
   // Phase 3: totals, offsets and this block's bases from the whole table.
   // Thread i reads 4 experts (quad i % n_quads) of the table rows
   // bb = i / n_quads, i / n_quads + n_groups, ... with 16-byte loads.
-  for (int e = threadIdx.x; e < E_local; e += blockDim.x) {
-    s_base[e] = 0;
-    s_run[e] = 0;
-  }
-  __syncthreads();
   {
     const int n_quads = e_pad / 4;
     const int n_groups = max(1, static_cast<int>(blockDim.x) / n_quads);
@@ -154,7 +166,7 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
       const int q = i % n_quads;
       const int g = i / n_quads;
       int4 tot = make_int4(0, 0, 0, 0), bef = make_int4(0, 0, 0, 0);
-#pragma unroll 4
+#pragma unroll 8
       for (int bb = g; bb < B; bb += n_groups) {
         const int4 c =
             __ldcg(reinterpret_cast<const int4*>(table + static_cast<int64_t>(bb) * e_pad) + q);
@@ -167,8 +179,8 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         if (e0 + u < E_local) {
-          atomicAdd(&s_base[e0 + u], tv[u]);
-          atomicAdd(&s_run[e0 + u], bv[u]);
+          atomicAdd(&s_tot[e0 + u], tv[u]);
+          atomicAdd(&s_bef[e0 + u], bv[u]);
         }
       }
     }
@@ -182,7 +194,7 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int e = threadIdx.x * kPer + u;
-      tot[u] = e < E_local ? s_base[e] : 0;
+      tot[u] = e < E_local ? s_tot[e] : 0;
       sum += tot[u];
     }
     int n_valid;
@@ -191,7 +203,7 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
     for (int u = 0; u < kPer; ++u) {
       const int e = threadIdx.x * kPer + u;
       if (e < E_local) {
-        s_base[e] = run + s_run[e];
+        s_base[e] = run + s_bef[e];
         if (b == 0) offsets[e] = run;
       }
       run += tot[u];
