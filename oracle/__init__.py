@@ -71,6 +71,10 @@ class OracleLib:
         lib.oracle_unpermute.argtypes = [P, I64, P, P, I64, I64, I32, P]
         lib.oracle_f32_to_bf16_rne.restype = None
         lib.oracle_f32_to_bf16_rne.argtypes = [P, I64, P]
+        lib.oracle_f32_to_e4m3.restype = None
+        lib.oracle_f32_to_e4m3.argtypes = [P, I64, P]
+        lib.oracle_quantize_fp8.restype = None
+        lib.oracle_quantize_fp8.argtypes = [P, I64, I64, I64, P, P]
         self.lib = lib
         self.path = path
 
@@ -83,6 +87,23 @@ class OracleLib:
 
     def f32_to_bf16_rne(self, x):
         return _f32_to_bf16_rne(self.lib, x)
+
+    def f32_to_e4m3(self, x):
+        x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
+        out = np.zeros(x.shape[0], np.uint8)
+        self.lib.oracle_f32_to_e4m3(_ptr(x), x.shape[0], _ptr(out))
+        return out
+
+    def quantize_fp8(self, x_bf16_bits, group=128):
+        """bf16 rows [T, H] (uint16 bits) -> (e4m3 codes uint8 [T, H],
+        fp32 scales [T, H / group])."""
+        x = np.ascontiguousarray(x_bf16_bits, dtype=np.uint16)
+        T, H = x.shape
+        assert H % group == 0
+        codes = np.zeros((T, H), np.uint8)
+        scales = np.zeros((T, H // group), np.float32)
+        self.lib.oracle_quantize_fp8(_ptr(x), T, H, group, _ptr(codes), _ptr(scales))
+        return codes, scales
 
 
 _default = None
@@ -114,6 +135,16 @@ def unpermute(rows_bf16_bits, topk_weights, inv_permuted_idx):
 def f32_to_bf16_rne(x):
     """The oracle's hand-written fp32 -> bf16 rounding, exposed for pinning."""
     return _load().f32_to_bf16_rne(x)
+
+
+def f32_to_e4m3(x):
+    """The oracle's hand-written fp32 -> e4m3 (satfinite, RNE), for pinning."""
+    return _load().f32_to_e4m3(x)
+
+
+def quantize_fp8(x_bf16_bits, group=128):
+    """Per-token, per-group fp8 quantisation (see moe_oracle.c)."""
+    return _load().quantize_fp8(x_bf16_bits, group)
 
 
 def _permute(lib, topk_ids: np.ndarray, E: int, expert_map: np.ndarray | None,

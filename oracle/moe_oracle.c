@@ -36,6 +36,12 @@
  *  - Dropped rows get inv_permuted_idx[r] = -1 and do not appear in
  *    [0, N_valid); permuted_idx[p] = -1 for p in [N_valid, T*K).  Rows
  *    p >= N_valid of permuted_hidden are not written.
+ *  - Quantise-on-permute (the fp8 activation step before the fp8 grouped
+ *    GEMM; "[Kernels] MoE refactor" (vLLM PR #19636), bot summary: quant_dtype,
+ *    per_act_token_quant, block_shape): per token and 128-column group,
+ *    scale = amax / 448 (1 for an all-zero group), code = e4m3(x / scale) with
+ *    round-to-nearest-even and saturation at +-448; the permuted rows are
+ *    these codes and scales gathered like any other rows.
  *  - Unpermute: acc = 0.0f; for k = 0..K-1 in order, if inv[t*K+k] >= 0,
  *    acc = acc + w[t,k] * float(row) (fp32 multiply, then fp32 add); the
  *    result is rounded once to bf16, round-to-nearest-even.  A token with no
@@ -44,6 +50,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include <math.h>
 
 #define ORC_FLAG_ID_RANGE  1u
 #define ORC_FLAG_MAP_RANGE 2u
@@ -225,4 +232,84 @@ void oracle_f32_to_bf16_rne(const float *x, int64_t n, uint16_t *out)
 {
     for (int64_t i = 0; i < n; ++i)
         out[i] = orc_f32_to_bf16_rne(x[i]);
+}
+
+/*
+ * fp32 -> fp8 e4m3 ("fn" variant: no infinities, 0x7F/0xFF are NaN, largest
+ * finite value 448 = 1.75 * 2^8), round to nearest, ties to even, saturating
+ * finite values beyond 448 to +-448.  Written from the format: normal codes
+ * are (exponent + 7) << 3 | mantissa for 2^-6 <= |v| < 2^9, subnormal codes
+ * count multiples of 2^-9 below 2^-6.  Exact in double: every scaling below
+ * is by a power of two.
+ */
+static double orc_round_half_even(double v) /* v >= 0 */
+{
+    double fl = (double)(long long)v;
+    double frac = v - fl;
+    if (frac > 0.5 || (frac == 0.5 && ((long long)fl & 1)))
+        fl += 1.0;
+    return fl;
+}
+
+static uint8_t orc_f32_to_e4m3_satfinite(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint8_t sign = (uint8_t)((u >> 31) << 7);
+    if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x007fffffu) != 0)
+        return (uint8_t)(sign | 0x7f); /* NaN */
+    double a = fabs((double)f);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7e); /* saturate (also +-inf) */
+    if (a < 0.015625) { /* below 2^-6: subnormal grid of 2^-9 */
+        double m = orc_round_half_even(a * 512.0); /* 0..8; 8 is the smallest normal */
+        return (uint8_t)(sign | (uint8_t)m);
+    }
+    int e = 0;
+    double t = a;
+    while (t >= 2.0) { t *= 0.5; e += 1; }
+    while (t < 1.0) { t *= 2.0; e -= 1; }
+    double m8 = orc_round_half_even(t * 8.0); /* 8..16 */
+    if (m8 == 16.0) { m8 = 8.0; e += 1; }
+    if (e > 8 || (e == 8 && m8 > 14.0))
+        return (uint8_t)(sign | 0x7e);
+    return (uint8_t)(sign | (uint8_t)(((e + 7) << 3) | ((int)m8 - 8)));
+}
+
+/* The conversion alone, exposed so tests can pin it directly. */
+void oracle_f32_to_e4m3(const float *x, int64_t n, uint8_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_f32_to_e4m3_satfinite(x[i]);
+}
+
+/*
+ * Per-token, per-group fp8 quantisation of bf16 rows (the activation format
+ * the fp8 grouped GEMM reads: per-token quantisation in column groups):
+ *   amax  = max |x| over the group's elements (0 if all are zero),
+ *   scale = amax / 448 (fp32 division), or 1 when amax == 0,
+ *   code  = e4m3(x / scale) (fp32 division, then the conversion above).
+ * x: [T, H] bf16 bits; codes: [T, H] e4m3; scales: [T, H / group] fp32.
+ * H must be a multiple of group.
+ */
+void oracle_quantize_fp8(const uint16_t *x, int64_t T, int64_t H, int64_t group,
+                         uint8_t *codes, float *scales)
+{
+    int64_t n_groups = H / group;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t g = 0; g < n_groups; ++g) {
+            const uint16_t *xg = x + t * H + g * group;
+            float amax = 0.0f;
+            for (int64_t i = 0; i < group; ++i) {
+                float v = fabsf(orc_bf16_to_f32(xg[i]));
+                if (v > amax)
+                    amax = v;
+            }
+            float scale = amax > 0.0f ? amax / 448.0f : 1.0f;
+            scales[t * n_groups + g] = scale;
+            for (int64_t i = 0; i < group; ++i)
+                codes[t * H + g * group + i] =
+                    orc_f32_to_e4m3_satfinite(orc_bf16_to_f32(xg[i]) / scale);
+        }
+    }
 }

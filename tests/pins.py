@@ -343,7 +343,112 @@ def pin_flags(orc):
     assert f == 4
 
 
+# ------------------------------------------------------ fp8 quantisation ---
+
+def e4m3_value(c):
+    """Value of one e4m3 ("fn") code, from the format: sign, 4-bit exponent
+    (bias 7), 3-bit mantissa; exponent 0 is subnormal; 0x7F / 0xFF are NaN."""
+    sign = -1.0 if c & 0x80 else 1.0
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    if e == 15 and m == 7:
+        return float("nan")
+    if e == 0:
+        return sign * (m / 8.0) * 2.0 ** -6
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+def pin_e4m3_exhaustive(orc):
+    """Every finite code decodes and re-encodes to itself (signed zero kept)."""
+    codes = [c for c in range(256) if c not in (0x7F, 0xFF)]
+    vals = np.array([e4m3_value(c) for c in codes], np.float64)
+    x = vals.astype(np.float32)
+    assert np.array_equal(x.astype(np.float64), vals)  # all exact in fp32
+    x[codes.index(0x80)] = np.float32(-0.0)
+    got = orc.f32_to_e4m3(x)
+    assert got.tolist() == codes
+
+
+def pin_e4m3_ties_and_neighbours(orc):
+    """Midpoints between neighbouring finite values go to the even code;
+    points just off a midpoint go to the nearer code."""
+    pos = [c for c in range(0x7F) if c != 0x7F]
+    for c in pos[:-1]:
+        lo, hi = e4m3_value(c), e4m3_value(c + 1)
+        mid = (lo + hi) / 2.0
+        even = c if (c & 1) == 0 else c + 1
+        x = np.array([mid, np.nextafter(np.float32(mid), np.float32(0)),
+                      np.nextafter(np.float32(mid), np.float32(1e9))], np.float32)
+        assert float(x[0]) == mid
+        got = orc.f32_to_e4m3(x).tolist()
+        assert got == [even, c, c + 1], (c, got)
+        neg = orc.f32_to_e4m3(-x).tolist()
+        assert neg == [even | 0x80, c | 0x80, (c + 1) | 0x80]
+
+
+def pin_e4m3_vs_torch_and_saturation(orc, seed=8):
+    rng = np.random.default_rng(seed)
+    x = np.concatenate([rng.standard_normal(100000) * 50, rng.uniform(-448, 448, 100000),
+                        rng.standard_normal(50000) * 1e-3]).astype(np.float32)
+    got = orc.f32_to_e4m3(x)
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, want)
+    big = np.array([448.0, 449.0, 463.9, 464.0, 500.0, 1e30, np.inf], np.float32)
+    assert orc.f32_to_e4m3(big).tolist() == [0x7E] * 7
+    assert orc.f32_to_e4m3(-big).tolist() == [0xFE] * 7
+    nan = orc.f32_to_e4m3(np.array([np.nan, -np.nan], np.float32)).tolist()
+    assert [c & 0x7F for c in nan] == [0x7F, 0x7F]
+
+
+def pin_quantize_golden(orc):
+    g = load_golden()["quantize_fp8"]
+    G = g["group"]
+    groups = g["groups"]
+    x = np.zeros((1, G * len(groups)), np.float32)
+    for gi, grp in enumerate(groups):
+        for i, v in grp["nonzero"].items():
+            x[0, gi * G + int(i)] = v
+    bits = f64_to_bf16_bits_exact(x)
+    codes, scales = orc.quantize_fp8(bits, G)
+    for gi, grp in enumerate(groups):
+        want = np.zeros(G, np.uint8)
+        for i, c in grp["codes_nonzero"].items():
+            want[int(i)] = c
+        assert codes[0, gi * G:(gi + 1) * G].tolist() == want.tolist(), grp["name"]
+        expr = grp["scale_is"]
+        if expr == "1":
+            assert scales[0, gi] == np.float32(1.0)
+        else:
+            num = float(expr.split("fp32(")[1].split(")")[0])
+            assert scales[0, gi] == np.float32(num) / np.float32(448.0), grp["name"]
+
+
+def pin_quantize_properties(orc, seed=9):
+    rng = np.random.default_rng(seed)
+    T, H, G = 37, 512, 128
+    x = rng.standard_normal((T, H)).astype(np.float32) * rng.uniform(0.01, 100, (T, 1)).astype(np.float32)
+    x[3, 128:256] = 0.0  # an all-zero group
+    bits = torch_bf16_bits(x)
+    xb = bf16_bits_to_f64(bits)
+    codes, scales = orc.quantize_fp8(bits, G)
+    vals = np.vectorize(e4m3_value)(codes.astype(np.int64))
+    deq = vals * np.repeat(scales.astype(np.float64), G, axis=1)
+    amax = np.abs(xb).reshape(T, H // G, G).max(axis=2)
+    nz = amax > 0
+    assert np.all(scales[~nz] == 1.0) and np.all(codes.reshape(T, H // G, G)[~nz] == 0)
+    assert np.array_equal(scales[nz], (amax[nz].astype(np.float32) / np.float32(448.0)))
+    top = np.abs(vals).reshape(T, H // G, G).max(axis=2)
+    assert np.all(top[nz] == 448.0)
+    s = np.repeat(scales.astype(np.float64), G, axis=1)
+    # half an e4m3 ulp (2^-4 relative) of the scaled value, or half the
+    # subnormal step (2^-10 * scale), plus the fp32 division's own rounding
+    bound = np.maximum(np.abs(xb) * 2.0 ** -4, s * 2.0 ** -10) * (1 + 2.0 ** -20)
+    assert np.all(np.abs(deq - xb) <= bound)
+
+
 ALL_PINS = [pin_golden_routing, pin_golden_unpermute, pin_golden_rounding,
             pin_rounding_vs_torch, pin_brute_random, pin_exhaustive_tiny,
             pin_invariants, pin_closed_forms, pin_rows_copied,
-            pin_unpermute_one_hot, pin_unpermute_bound, pin_flags]
+            pin_unpermute_one_hot, pin_unpermute_bound, pin_flags,
+            pin_e4m3_exhaustive, pin_e4m3_ties_and_neighbours,
+            pin_e4m3_vs_torch_and_saturation, pin_quantize_golden, pin_quantize_properties]

@@ -31,6 +31,16 @@ MUTANTS = {
     "ties_away_from_zero": ("(dropped == 0x8000u && (kept & 1u))", "(dropped == 0x8000u)"),
     "subtract_term": ("acc = acc + prod;", "acc = acc - prod;"),
     "scale_row_wrong_token": ("scales + t * scale_cols", "scales + (t / 2) * scale_cols"),
+    "e4m3_ties_away": ("if (frac > 0.5 || (frac == 0.5 && ((long long)fl & 1)))",
+                       "if (frac >= 0.5)"),
+    "e4m3_truncate": ("double m8 = orc_round_half_even(t * 8.0);", "double m8 = (double)(long long)(t * 8.0);"),
+    "e4m3_no_saturation": ("        return (uint8_t)(sign | 0x7e); /* saturate (also +-inf) */",
+                           "        return (uint8_t)(sign | 0x7f); /* saturate (also +-inf) */"),
+    "e4m3_subnormal_grid": ("double m = orc_round_half_even(a * 512.0);", "double m = orc_round_half_even(a * 256.0);"),
+    "quant_wrong_max": ("float scale = amax > 0.0f ? amax / 448.0f : 1.0f;",
+                        "float scale = amax > 0.0f ? amax / 240.0f : 1.0f;"),
+    "quant_zero_group_scale": ("float scale = amax > 0.0f ? amax / 448.0f : 1.0f;",
+                               "float scale = amax > 0.0f ? amax / 448.0f : 0.0f;"),
 }
 
 CHILD = r"""
