@@ -64,6 +64,12 @@ def gather_kernel_bytes(T, H, K, elem, scale_cols, Tv, Nv):
     return T * K * 4 + Tv * rb + Nv * rb
 
 
+def quant_permute_bytes(T, H, K, E_L, Tv, Nv, group=128):
+    """ids + bf16 source rows read once + fp8 codes and fp32 scales written to
+    every kept row + both index maps + offsets."""
+    return T * K * 4 + Tv * H * 2 + Nv * (H + (H // group) * 4) + 2 * T * K * 4 + (E_L + 1) * 8
+
+
 def unpermute_bytes(T, H, K, Nv):
     """inv + weights + kept expert rows read + output written."""
     return 2 * T * K * 4 + Nv * H * 2 + T * H * 2
@@ -201,6 +207,22 @@ class Setup:
         self.gbytes = gather_kernel_bytes(T, wl.H, wl.K, elem, sc, self.Tv, self.Nv)
         self.ubytes = unpermute_bytes(T, wl.H, wl.K, self.Nv)
 
+    def enable_quant(self, dev):
+        """bf16 rows of the same shape and fp8 outputs for quantise-on-permute."""
+        g = torch.Generator(device=dev).manual_seed(1234)
+        R = self.T * self.wl.K
+        self.qhidden = torch.randn(self.T, self.wl.H, generator=g, device=dev,
+                                   dtype=torch.bfloat16)
+        self.qcodes = torch.empty(R, self.wl.H, dtype=torch.float8_e4m3fn, device=dev)
+        self.qscales = torch.empty(R, self.wl.H // 128, dtype=torch.float32, device=dev)
+        self.qbytes = quant_permute_bytes(self.T, self.wl.H, self.wl.K, self.wl.e_local,
+                                          self.Tv, self.Nv)
+
+    def permute_quant(self):
+        self.mp.moe_permute_quant_fp8(self.qhidden, self.ids, self.offsets, self.pidx, self.inv,
+                                      self.ws, self.qcodes, self.qscales, num_experts=self.wl.E,
+                                      num_local_experts=self.wl.e_local, expert_map=self.emap)
+
     def permute(self):
         self.mp.moe_permute(self.hidden, self.ids, self.offsets, self.pidx, self.inv, self.ws,
                             num_experts=self.wl.E, num_local_experts=self.wl.e_local,
@@ -284,7 +306,8 @@ def sweep(dev, peak, flush):
     sets for the smallest batches).  *_us is the device time per call from
     replaying a CUDA graph of back-to-back calls (no Python launch cost);
     *_eager_us the same calls launched one by one from Python; at T = 1 also a
-    single eager call after an L2 flush."""
+    single eager call after an L2 flush.  For the DeepSeek-V3 shape also
+    quantise-on-permute from bf16 rows (quant_fp8_permute_*)."""
     rows = []
     for name, wl in WORKLOADS.items():
         if name == "tiny":
@@ -306,6 +329,13 @@ def sweep(dev, peak, flush):
                    "unpermute_frac": round(s0.ubytes / u_us / 1e3 / peak, 4),
                    "permute_eager_us": round(back_to_back_us([s.permute for s in sets], n), 2),
                    "unpermute_eager_us": round(back_to_back_us([s.unpermute for s in sets], n), 2)}
+            if name == "dsv3":
+                for st in sets:
+                    st.enable_quant(dev)
+                q_us = graph_us([st.permute_quant for st in sets], n_graph)
+                rec["quant_fp8_permute_us"] = round(q_us, 2)
+                rec["quant_fp8_permute_GBps"] = round(s0.qbytes / q_us / 1e3, 1)
+                rec["quant_fp8_permute_frac"] = round(s0.qbytes / q_us / 1e3 / peak, 4)
             if T == 1:
                 rec["permute_after_flush_us"] = round(timed_calls(s0.permute, 50, flush), 2)
                 rec["unpermute_after_flush_us"] = round(timed_calls(s0.unpermute, 50, flush), 2)

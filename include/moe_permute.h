@@ -167,6 +167,35 @@ MOE_API int moe_permute(const void *hidden_states, moe_dtype_t hidden_dtype,
                 moe_stream_t stream);
 
 /*
+ * moe_permute_quant_fp8: moe_permute for bf16 activations that feed an fp8
+ * grouped GEMM, with the quantisation done during the row gather instead of
+ * in a separate pass ("[Kernels] MoE refactor" (vLLM PR #19636), bot summary:
+ * activation quantisation parameters quant_dtype, per_act_token_quant,
+ * block_shape).  Per token and per MOE_QUANT_GROUP-column group:
+ *   scale = amax(|x|) / 448 (fp32 division; 1 for an all-zero group),
+ *   code  = e4m3(x / scale) (fp32 division, round to nearest even,
+ *           saturating at +-448),
+ * and permuted row p gets the codes and scales of its token.
+ *
+ *  hidden_states    [T, H] bf16, 16-byte aligned, H a multiple of MOE_QUANT_GROUP.
+ *  permuted_codes   [R, H] fp8 e4m3 (bytes), 8-byte aligned.
+ *  permuted_scales  [R, H / MOE_QUANT_GROUP] fp32.
+ *  Every other argument, the metadata outputs, the workspace rules and the
+ *  dropped-row rules are those of moe_permute.  Rows p >= N_valid of the codes
+ *  and scales are not written.
+ */
+#define MOE_QUANT_GROUP 128
+MOE_API int moe_permute_quant_fp8(const void *hidden_states, const void *topk_ids,
+                                  moe_index_t topk_ids_dtype, const int32_t *expert_map,
+                                  int64_t num_tokens, int64_t hidden_size, int32_t topk,
+                                  int32_t num_experts, int32_t num_local_experts,
+                                  void *permuted_codes, float *permuted_scales,
+                                  int64_t *expert_first_token_offset,
+                                  int32_t *permuted_idx, int32_t *inv_permuted_idx,
+                                  void *workspace, size_t workspace_bytes,
+                                  moe_stream_t stream);
+
+/*
  * moe_unpermute: out[t] = bf16_rne( sum over k = 0..K-1 in order, skipping
  * rows with inv_permuted_idx[t*K+k] == -1, of topk_weights[t,k] *
  * permuted_rows[inv_permuted_idx[t*K+k]] ), accumulated in fp32 with a

@@ -95,6 +95,28 @@ def moe_permute(hidden_states, topk_ids, expert_first_token_offset, permuted_idx
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
+def moe_permute_quant_fp8(hidden_states, topk_ids, expert_first_token_offset, permuted_idx,
+                          inv_permuted_idx, workspace, permuted_codes, permuted_scales, *,
+                          num_experts, num_local_experts=None, expert_map=None,
+                          stream=None) -> None:
+    """Permute bf16 rows and quantise them to fp8 e4m3 on the way (see
+    include/moe_permute.h): permuted_codes [T*K, H] float8_e4m3fn,
+    permuted_scales [T*K, H/128] float32."""
+    T, K = topk_ids.shape
+    if hidden_states.dtype != torch.bfloat16:
+        raise ValueError("moe_permute_quant_fp8 takes bf16 hidden_states")
+    if permuted_codes.dtype not in (torch.float8_e4m3fn, torch.uint8):
+        raise ValueError("permuted_codes must be float8_e4m3fn (or raw uint8)")
+    if num_local_experts is None:
+        num_local_experts = num_experts
+    _b.check("moe_permute_quant_fp8", _b.lib().moe_permute_quant_fp8(
+        _ptr(hidden_states), _ptr(topk_ids), _INDEX[topk_ids.dtype], _ptr(expert_map),
+        T, hidden_states.shape[1], K, num_experts, num_local_experts,
+        _ptr(permuted_codes), _ptr(permuted_scales), _ptr(expert_first_token_offset),
+        _ptr(permuted_idx), _ptr(inv_permuted_idx), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
 def moe_unpermute(permuted_rows, topk_weights, inv_permuted_idx, out, *, workspace=None,
                   stream=None) -> None:
     """out[t] = bf16(sum_k w[t,k] * permuted_rows[inv[t*K+k]]) in place.

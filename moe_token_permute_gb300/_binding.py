@@ -33,6 +33,7 @@ MOE_FLAG_INV_OUT_OF_RANGE = 4
 
 MOE_MAX_TOPK = 32
 MOE_MAX_LOCAL_EXPERTS = 1024
+MOE_QUANT_GROUP = 128
 
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
@@ -51,6 +52,8 @@ SIGNATURES = {
     "moe_unpermute": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I32, _P, _P, _P]),
     "moe_read_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
     "moe_clear_status": (ctypes.c_int, [_P, _P]),
+    "moe_permute_quant_fp8": (ctypes.c_int, [_P, _P, ctypes.c_int, _P, _I64, _I64, _I32, _I32,
+                                             _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _P, _I64, _P, ctypes.c_int, _P,
                                            _I64, _I64, _I32, _I32, _I32,
                                            _P, _P, _P, _P, _P, _P]),

@@ -27,6 +27,7 @@
 #include "routing.cuh"
 #include "rows.cuh"
 #include "route_coop.cuh"
+#include "quant.cuh"
 
 namespace moe {
 namespace {
@@ -244,6 +245,24 @@ cudaError_t permute_typed(const IdT* ids, const int32_t* emap, int64_t T, int K,
   }
 }
 
+constexpr int kQuantV = 4;  // vectors of 8 bf16 per lane in one quantise item (8 groups)
+
+template <typename IdT>
+cudaError_t permute_quant_typed(const IdT* ids, const int32_t* emap, int64_t T, int K, int E,
+                                int E_local, const void* hidden, int64_t H, void* codes,
+                                float* scales, int64_t* offsets, int32_t* pidx, int32_t* inv,
+                                void* ws, const DeviceInfo* d, cudaStream_t s) {
+  cudaError_t err = launch_route<IdT>(ids, emap, T, K, E, E_local, offsets, pidx, inv,
+                                      static_cast<WsHeader*>(ws), d, s);
+  if (err != cudaSuccess) return err;
+  const int64_t row_vecs = H / 8;
+  const int64_t blocks = ceil_div(row_items(T, row_vecs, kQuantV), kRowWarps);
+  if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
+  return launch(k_gather_quant_fp8<kQuantV>, static_cast<unsigned>(blocks), kRowThreads, 0, s,
+                static_cast<const uint4*>(hidden), row_vecs, static_cast<const int32_t*>(inv), T,
+                K, static_cast<uint2*>(codes), scales);
+}
+
 template <typename VecT, int KG, int V>
 cudaError_t launch_unpermute_kv(const void* rows, int64_t num_rows, int64_t H, const float* w,
                                 const int32_t* inv, int64_t T, int K, void* out,
@@ -386,6 +405,58 @@ int moe_permute(const void* hidden_states, moe_dtype_t hidden_dtype, const float
                                  hidden_scales, scale_cols, permuted_hidden_states,
                                  permuted_scales, expert_first_token_offset, permuted_idx,
                                  inv_permuted_idx, workspace, d, s);
+  }
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_permute_quant_fp8(const void* hidden_states, const void* topk_ids,
+                          moe_index_t topk_ids_dtype, const int32_t* expert_map,
+                          int64_t num_tokens, int64_t hidden_size, int32_t topk,
+                          int32_t num_experts, int32_t num_local_experts, void* permuted_codes,
+                          float* permuted_scales, int64_t* expert_first_token_offset,
+                          int32_t* permuted_idx, int32_t* inv_permuted_idx, void* workspace,
+                          size_t workspace_bytes, moe_stream_t stream) {
+  const int64_t T = num_tokens, H = hidden_size;
+  if (T < 0 || H < MOE_QUANT_GROUP || H % MOE_QUANT_GROUP != 0 || topk < 1 ||
+      topk > MOE_MAX_TOPK || num_experts < 1 || num_local_experts < 1 ||
+      num_local_experts > num_experts || num_local_experts > MOE_MAX_LOCAL_EXPERTS)
+    return MOE_ERR_INVALID_ARG;
+  if (expert_map == nullptr && num_local_experts != num_experts) return MOE_ERR_INVALID_ARG;
+  if (topk_ids_dtype != MOE_INDEX_INT32 && topk_ids_dtype != MOE_INDEX_INT64)
+    return MOE_ERR_INVALID_ARG;
+  if (T > INT32_MAX / topk || H > INT64_MAX / 64) return MOE_ERR_INVALID_ARG;
+  if (expert_first_token_offset == nullptr || !aligned(expert_first_token_offset, 8))
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0) {
+    const size_t id_bytes = topk_ids_dtype == MOE_INDEX_INT64 ? 8 : 4;
+    if (topk_ids == nullptr || !aligned(topk_ids, id_bytes)) return MOE_ERR_INVALID_ARG;
+    if (expert_map != nullptr && !aligned(expert_map, 4)) return MOE_ERR_INVALID_ARG;
+    if (permuted_idx == nullptr || inv_permuted_idx == nullptr || !aligned(permuted_idx, 4) ||
+        !aligned(inv_permuted_idx, 4))
+      return MOE_ERR_INVALID_ARG;
+    if (hidden_states == nullptr || !aligned(hidden_states, 16) || permuted_codes == nullptr ||
+        !aligned(permuted_codes, 8) || permuted_scales == nullptr || !aligned(permuted_scales, 4))
+      return MOE_ERR_INVALID_ARG;
+    if (workspace == nullptr || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < workspace_bytes_for(T, topk, num_experts))
+      return MOE_ERR_WORKSPACE_TOO_SMALL;
+  }
+  const DeviceInfo* d = current_device();
+  if (!is_supported(d)) return MOE_ERR_UNSUPPORTED_DEVICE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (T == 0) {
+    err = launch(k_zero_offsets, 1, 256, 0, s, expert_first_token_offset, num_local_experts + 1);
+  } else if (topk_ids_dtype == MOE_INDEX_INT32) {
+    err = permute_quant_typed<int32_t>(static_cast<const int32_t*>(topk_ids), expert_map, T, topk,
+                                       num_experts, num_local_experts, hidden_states, H,
+                                       permuted_codes, permuted_scales, expert_first_token_offset,
+                                       permuted_idx, inv_permuted_idx, workspace, d, s);
+  } else {
+    err = permute_quant_typed<int64_t>(static_cast<const int64_t*>(topk_ids), expert_map, T, topk,
+                                       num_experts, num_local_experts, hidden_states, H,
+                                       permuted_codes, permuted_scales, expert_first_token_offset,
+                                       permuted_idx, inv_permuted_idx, workspace, d, s);
   }
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -1,0 +1,94 @@
+// quant.cuh -- quantise-on-permute: bf16 rows in, fp8 e4m3 rows plus fp32
+// per-token, per-128-column scales out, written straight to each row's K
+// destinations.
+//
+// The fp8 grouped GEMM after the permute reads per-token, per-column-group
+// quantised activations ("[Kernels] MoE refactor" (vLLM PR #19636), bot
+// summary: quant_dtype, per_act_token_quant, block_shape).  Quantising inside
+// the gather saves a separate pass over the activations:
+//   scale = amax(|x| over the group) / 448   (1 when the group is all zero),
+//   code  = e4m3(x / scale), round to nearest even, saturating at +-448.
+// Both divisions are IEEE-rounded fp32 divisions.
+//
+// Layout: a warp owns one (token, chunk) item of 32 lanes x V vectors of 8
+// bf16 values.  Vector c of a row belongs to column group c / 16, so for each
+// vector slot i the lanes 0-15 hold one 128-column group and lanes 16-31 the
+// next: the group's amax is a 4-step max-shuffle inside a half warp.
+#pragma once
+
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kQuantGroup = 128;  // columns per scale
+constexpr float kE4m3Max = 448.0f;
+
+template <int V>
+__global__ void __launch_bounds__(256)
+k_gather_quant_fp8(const uint4* __restrict__ hidden, int64_t row_vecs,
+                   const int32_t* __restrict__ inv_permuted_idx, int64_t T, int K,
+                   uint2* __restrict__ out_codes, float* __restrict__ out_scales) {
+  constexpr int64_t kChunk = 32 * V;  // vectors of 8 values per item
+  const int lane = threadIdx.x & 31;
+  const int64_t n_chunks = (row_vecs + kChunk - 1) / kChunk;
+  const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (item >= T * n_chunks) return;
+  const int64_t t = item / n_chunks;
+  const int64_t c0 = (item - t * n_chunks) * kChunk;
+  const int64_t n_groups = row_vecs / (kQuantGroup / 8);
+
+  uint4 v[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int64_t c = c0 + i * 32 + lane;
+    v[i] = c < row_vecs ? ld_stream(hidden + t * row_vecs + c) : make_uint4(0, 0, 0, 0);
+  }
+  // The rows are the caller's input (complete: the routing grid has passed its
+  // own dependency wait); the positions come from the routing grid.
+  pdl_wait();
+  int p = lane < K ? __ldcg(inv_permuted_idx + t * K + lane) : -1;
+  if (p >= T * K) p = -1;  // only a routing grid that gave up leaves such values
+  const unsigned valid = __ballot_sync(kFullMask, p >= 0);
+  if (valid == 0u) return;
+
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int64_t c = c0 + i * 32 + lane;
+    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+    float x[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(h2[j]);
+      x[2 * j] = f.x;
+      x[2 * j + 1] = f.y;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[j]));
+#pragma unroll
+    for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, d));
+    const float scale = amax > 0.0f ? __fdiv_rn(amax, kE4m3Max) : 1.0f;
+    uint2 packed;
+    unsigned short* q2 = reinterpret_cast<unsigned short*>(&packed);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = make_float2(__fdiv_rn(x[2 * j], scale), __fdiv_rn(x[2 * j + 1], scale));
+      q2[j] = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+    }
+    const int64_t g = c / (kQuantGroup / 8);
+    unsigned m = valid;
+    while (m != 0u) {
+      const int k = __ffs(m) - 1;
+      m &= m - 1u;
+      const int pk = __shfl_sync(kFullMask, p, k);
+      if (c < row_vecs) {
+        out_codes[static_cast<int64_t>(pk) * row_vecs + c] = packed;
+        if ((lane & 15) == 0) out_scales[static_cast<int64_t>(pk) * n_groups + g] = scale;
+      }
+    }
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,136 @@
+"""GPU parity of quantise-on-permute (moe_permute_quant_fp8) against the CPU
+oracle: the oracle quantises every token row (per-token, per-128-column fp8
+e4m3) and then permutes the codes and scales like any other rows.  Codes,
+scales, offsets and both index maps must match bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import moe_token_permute_gb300 as mp
+import oracle
+from gpu_util import alloc_outputs, assert_metadata_equal, bits16, bytes_of
+from moe_token_permute_gb300.workloads import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+G = mp._binding.MOE_QUANT_GROUP
+
+
+def bf16_rows(T, H, seed, device="cpu"):
+    """bf16 N(0,1) rows with per-token magnitudes spread over ~2 decades, plus
+    planted corner cases: an all-zero group, a tiny-valued group (e4m3
+    subnormal codes) and a group with one large spike."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    x = torch.randn(T, H, generator=g, device=device)
+    x = x * torch.exp(torch.randn(T, 1, generator=g, device=device))
+    if T > 0 and H >= 3 * G:
+        x[0, 0:G] = 0.0
+        x[0, G:2 * G] *= 1e-4
+        x[T - 1, 2 * G:3 * G] *= 1e-3
+        x[T - 1, 2 * G + 5] = 300.0
+    return x.to(torch.bfloat16).contiguous()
+
+
+def run_quant(hidden, inp, ids_dtype=torch.int32):
+    wl = inp["wl"]
+    T = hidden.shape[0]
+    H = hidden.shape[1]
+    bufs = alloc_outputs(T, wl.K, wl.e_local, E=wl.E)
+    R = T * wl.K
+    codes = torch.zeros(R, H, dtype=torch.uint8, device="cuda")
+    scales = torch.zeros(R, H // G, dtype=torch.float32, device="cuda")
+    emap = None if inp["expert_map"] is None else inp["expert_map"].cuda()
+    mp.moe_permute_quant_fp8(hidden.cuda(), inp["topk_ids"].to(device="cuda", dtype=ids_dtype),
+                             bufs["offsets"], bufs["pidx"], bufs["inv"], bufs["ws"], codes, scales,
+                             num_experts=wl.E, num_local_experts=wl.e_local, expert_map=emap)
+    return bufs, codes, scales
+
+
+def oracle_quant_permute(hidden, inp):
+    wl = inp["wl"]
+    q, s = oracle.quantize_fp8(bits16(hidden), G)
+    return oracle.permute(inp["topk_ids"].cpu().numpy(), wl.E,
+                          expert_map=None if inp["expert_map"] is None else inp["expert_map"].cpu().numpy(),
+                          E_local=wl.e_local, hidden=q, scales=s)
+
+
+CASES = [("dsv3", 1), ("dsv3", 128), ("dsv3", 4096), ("qwen3", 1024), ("mixtral", 512),
+         ("dsv2lite", 256), ("dsv2lite", 8192), ("tiny", 16)]
+
+
+@pytest.mark.parametrize("name,T", CASES, ids=[f"{n}-T{T}" for n, T in CASES])
+def test_quant_permute_matches_oracle(name, T):
+    inp = make_inputs(name, T, seed=5, with_rows=False)
+    hidden = bf16_rows(T, WORKLOADS[name].H, seed=T + 7)
+    ref = oracle_quant_permute(hidden, inp)
+    bufs, codes, scales = run_quant(hidden, inp)
+    assert_metadata_equal(bufs, ref)
+    n = ref["n_valid"]
+    np.testing.assert_array_equal(bytes_of(codes[:n]), ref["permuted_hidden"][:n])
+    np.testing.assert_array_equal(scales[:n].cpu().numpy(), ref["permuted_scales"][:n])
+    assert mp.moe_read_status(bufs["ws"]) == 0
+
+
+def test_quant_permute_int64_ids_and_one_group_rows():
+    inp = make_inputs("qwen3", 300, seed=6, with_rows=False)
+    hidden = bf16_rows(300, G, seed=3)  # H = 128: a single group per row
+    ref = oracle_quant_permute(hidden, inp)
+    bufs, codes, scales = run_quant(hidden, inp, ids_dtype=torch.int64)
+    assert_metadata_equal(bufs, ref)
+    n = ref["n_valid"]
+    np.testing.assert_array_equal(bytes_of(codes[:n]), ref["permuted_hidden"][:n])
+    np.testing.assert_array_equal(scales[:n].cpu().numpy(), ref["permuted_scales"][:n])
+
+
+def test_quant_permute_large_sampled():
+    """The DeepSeek-V3-shaped layer at 32768 tokens (inputs drawn on the
+    device): metadata in full, codes and scales on sampled rows."""
+    T = 32768
+    inp = make_inputs("dsv3", T, seed=0, device="cuda", with_rows=False)
+    hidden = bf16_rows(T, WORKLOADS["dsv3"].H, seed=1, device="cuda")
+    bufs, codes, scales = run_quant(hidden, inp)
+    ids = inp["topk_ids"].cpu().numpy()
+    ref = oracle.permute(ids, WORKLOADS["dsv3"].E)
+    assert_metadata_equal(bufs, ref)
+    rng = np.random.default_rng(2)
+    n = ref["n_valid"]
+    ps = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 48)]))
+    toks = ref["permuted_idx"][ps] // WORKLOADS["dsv3"].K
+    q, s = oracle.quantize_fp8(bits16(hidden[torch.from_numpy(toks).cuda()]), G)
+    got_c = bytes_of(codes[torch.from_numpy(ps).cuda()])
+    got_s = scales[torch.from_numpy(ps).cuda()].cpu().numpy()
+    np.testing.assert_array_equal(got_c, q)
+    np.testing.assert_array_equal(got_s, s)
+
+
+def test_quant_permute_rejects_bad_shapes():
+    inp = make_inputs("tiny", 16, with_rows=False)
+    wl = inp["wl"]
+    bufs = alloc_outputs(16, wl.K, wl.E)
+    ids = inp["topk_ids"].cuda()
+    for H in (100, 64):  # not a whole number of 128-column groups
+        h = torch.zeros(16, H, dtype=torch.bfloat16, device="cuda")
+        c = torch.zeros(32, H, dtype=torch.uint8, device="cuda")
+        s = torch.zeros(32, 1, dtype=torch.float32, device="cuda")
+        with pytest.raises(mp.MoeError, match="invalid"):
+            mp.moe_permute_quant_fp8(h, ids, bufs["offsets"], bufs["pidx"], bufs["inv"], bufs["ws"],
+                                     c, s, num_experts=wl.E)
+    flat = torch.zeros(16 * 128 + 1, dtype=torch.bfloat16, device="cuda")
+    h = flat[1:].view(16, 128)  # 2-byte aligned only
+    c = torch.zeros(32, 128, dtype=torch.uint8, device="cuda")
+    s = torch.zeros(32, 1, dtype=torch.float32, device="cuda")
+    with pytest.raises(mp.MoeError, match="invalid"):
+        mp.moe_permute_quant_fp8(h, ids, bufs["offsets"], bufs["pidx"], bufs["inv"], bufs["ws"],
+                                 c, s, num_experts=wl.E)
+
+
+def test_quant_permute_zero_tokens():
+    inp = make_inputs("dsv3", 0, with_rows=False)
+    wl = inp["wl"]
+    bufs = alloc_outputs(0, wl.K, wl.E)
+    h = torch.zeros(0, wl.H, dtype=torch.bfloat16, device="cuda")
+    c = torch.zeros(0, wl.H, dtype=torch.uint8, device="cuda")
+    s = torch.zeros(0, wl.H // G, dtype=torch.float32, device="cuda")
+    mp.moe_permute_quant_fp8(h, inp["topk_ids"].cuda(), bufs["offsets"], bufs["pidx"], bufs["inv"],
+                             bufs["ws"], c, s, num_experts=wl.E)
+    assert bufs["offsets"].cpu().tolist() == [0] * (wl.E + 1)
