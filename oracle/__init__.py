@@ -36,6 +36,7 @@ _LIB_PATH = os.path.join(_OUT_DIR, "libmoe_oracle.so")
 FLAG_ID_RANGE = 1
 FLAG_MAP_RANGE = 2
 FLAG_INV_RANGE = 4
+FLAG_CAPACITY = 16
 
 
 def compile_source(src: str, out_path: str) -> str:
@@ -71,6 +72,9 @@ class OracleLib:
         lib.oracle_unpermute.argtypes = [P, I64, P, P, I64, I64, I32, P]
         lib.oracle_f32_to_bf16_rne.restype = None
         lib.oracle_f32_to_bf16_rne.argtypes = [P, I64, P]
+        lib.oracle_permute_batched.restype = ctypes.c_uint32
+        lib.oracle_permute_batched.argtypes = [P, I64, P, I64, P, ctypes.c_int, P, I64, I32,
+                                               I32, I32, I64, P, P, P, P]
         lib.oracle_f32_to_e4m3.restype = None
         lib.oracle_f32_to_e4m3.argtypes = [P, I64, P]
         lib.oracle_quantize_fp8.restype = None
@@ -87,6 +91,38 @@ class OracleLib:
 
     def f32_to_bf16_rne(self, x):
         return _f32_to_bf16_rne(self.lib, x)
+
+    def permute_batched(self, topk_ids, E, M, *, expert_map=None, E_local=None,
+                        hidden=None, scales=None):
+        """Batched layout: returns expert_num_tokens int32 [E_local],
+        inv_permuted_idx int32 [T*K] (slot e*M+j or -1), batched_hidden
+        [E_local*M, ...] and batched_scales (unused slots zero), flags."""
+        topk_ids = np.ascontiguousarray(topk_ids)
+        T, K = topk_ids.shape
+        if expert_map is None:
+            E_local = E if E_local is None else E_local
+        else:
+            expert_map = np.ascontiguousarray(expert_map, dtype=np.int32)
+        cnt = np.zeros(E_local, np.int32)
+        inv = np.zeros(T * K, np.int32)
+        bh, row_bytes = None, 0
+        if hidden is not None:
+            hidden = np.ascontiguousarray(hidden)
+            row_bytes = int(np.prod(hidden.shape[1:])) * hidden.itemsize
+            bh = np.zeros((E_local * M,) + hidden.shape[1:], hidden.dtype)
+        bs, scale_cols = None, 0
+        if scales is not None:
+            scales = np.ascontiguousarray(scales, dtype=np.float32)
+            scale_cols = scales.shape[1]
+            bs = np.zeros((E_local * M, scale_cols), np.float32)
+        flags = self.lib.oracle_permute_batched(
+            _ptr(hidden), row_bytes, _ptr(scales), scale_cols, _ptr(topk_ids),
+            int(topk_ids.dtype == np.int64), _ptr(expert_map), T, K, E, E_local, M,
+            _ptr(cnt), _ptr(inv), _ptr(bh), _ptr(bs))
+        if flags == 0xFFFFFFFF:
+            raise MemoryError("oracle_permute_batched: host allocation failed")
+        return dict(expert_num_tokens=cnt, inv_permuted_idx=inv, batched_hidden=bh,
+                    batched_scales=bs, flags=int(flags))
 
     def f32_to_e4m3(self, x):
         x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1)
@@ -135,6 +171,11 @@ def unpermute(rows_bf16_bits, topk_weights, inv_permuted_idx):
 def f32_to_bf16_rne(x):
     """The oracle's hand-written fp32 -> bf16 rounding, exposed for pinning."""
     return _load().f32_to_bf16_rne(x)
+
+
+def permute_batched(topk_ids, E, M, **kw):
+    """Batched-layout permute (see moe_oracle.c)."""
+    return _load().permute_batched(topk_ids, E, M, **kw)
 
 
 def f32_to_e4m3(x):

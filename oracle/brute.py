@@ -77,3 +77,30 @@ def unpermute_f32_sums(rows, w, inv, T, K, H):
             line.append(acc)
         out.append(line)
     return out
+
+
+def permute_batched(topk_ids, E, M, expert_map=None, E_local=None):
+    """Batched layout by the definition: the k-th row (in r order) routed to
+    local expert e lands in slot e*M + k if k < M, else it is dropped."""
+    T = len(topk_ids)
+    K = len(topk_ids[0]) if T else 0
+    if E_local is None:
+        E_local = E
+    placed = {e: [] for e in range(E_local)}
+    inv = [-1] * (T * K)
+    flags = 0
+    for t in range(T):
+        for k in range(K):
+            r = t * K + k
+            e, f = local_expert(int(topk_ids[t][k]), E, expert_map, E_local)
+            flags |= f
+            if e is None:
+                continue
+            if len(placed[e]) >= M:
+                flags |= 16
+                placed[e].append(None)
+                continue
+            inv[r] = e * M + len(placed[e])
+            placed[e].append(r)
+    counts = [min(len(placed[e]), M) for e in range(E_local)]
+    return dict(expert_num_tokens=counts, inv_permuted_idx=inv, flags=flags)

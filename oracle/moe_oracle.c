@@ -42,6 +42,12 @@
  *    scale = amax / 448 (1 for an all-zero group), code = e4m3(x / scale) with
  *    round-to-nearest-even and saturation at +-448; the permuted rows are
  *    these codes and scales gathered like any other rows.
+ *  - Batched layout (the modular kernel's second activation format, "[Kernels]
+ *    MoE refactor" (vLLM PR #19636), description: an activation-format enum
+ *    lets prepare/finalize and the experts agree on the layout): rows of local
+ *    expert e go to slots e*M + j, j = the row's stable rank inside the expert,
+ *    for a per-expert capacity M; rows with j >= M do not fit and are dropped
+ *    with ORC_FLAG_CAPACITY; expert_num_tokens[e] = min(count, M).
  *  - Unpermute: acc = 0.0f; for k = 0..K-1 in order, if inv[t*K+k] >= 0,
  *    acc = acc + w[t,k] * float(row) (fp32 multiply, then fp32 add); the
  *    result is rounded once to bf16, round-to-nearest-even.  A token with no
@@ -55,6 +61,7 @@
 #define ORC_FLAG_ID_RANGE  1u
 #define ORC_FLAG_MAP_RANGE 2u
 #define ORC_FLAG_INV_RANGE 4u
+#define ORC_FLAG_CAPACITY  16u
 
 /* Expert id of (t, k), widened to 64 bits whatever the storage type. */
 static int64_t orc_topk_id(const void *topk_ids, int ids_are_i64, int64_t r)
@@ -312,4 +319,54 @@ void oracle_quantize_fp8(const uint16_t *x, int64_t T, int64_t H, int64_t group,
                     orc_f32_to_e4m3_satfinite(orc_bf16_to_f32(xg[i]) / scale);
         }
     }
+}
+
+/*
+ * oracle_permute_batched: the batched layout.  Slots are [E_local, M] rows.
+ * inv_permuted_idx[r] = e*M + j, or -1 (dropped row, or no room: j >= M).
+ * expert_num_tokens: [E_local] int32 = min(rows routed to e, M).
+ * batched_hidden: [E_local*M, row_bytes] or NULL; batched_scales likewise.
+ * Slots j >= expert_num_tokens[e] are not written.
+ */
+uint32_t oracle_permute_batched(const void *hidden, int64_t row_bytes,
+                                const float *scales, int64_t scale_cols,
+                                const void *topk_ids, int ids_are_i64,
+                                const int32_t *expert_map,
+                                int64_t T, int32_t K, int32_t E, int32_t E_local,
+                                int64_t M, int32_t *expert_num_tokens,
+                                int32_t *inv_permuted_idx,
+                                void *batched_hidden, float *batched_scales)
+{
+    uint32_t flags = 0;
+    int64_t R = T * (int64_t)K;
+    int64_t *next = (int64_t *)calloc((size_t)E_local + 1, sizeof(int64_t));
+    if (!next)
+        return 0xffffffffu;
+    for (int64_t r = 0; r < R; ++r) {
+        int32_t e = orc_local_expert(topk_ids, ids_are_i64, expert_map, E,
+                                     E_local, r, &flags);
+        if (e < 0) {
+            inv_permuted_idx[r] = -1;
+            continue;
+        }
+        int64_t j = next[e]++;
+        if (j >= M) {
+            inv_permuted_idx[r] = -1;
+            flags |= ORC_FLAG_CAPACITY;
+            continue;
+        }
+        int64_t slot = (int64_t)e * M + j;
+        inv_permuted_idx[r] = (int32_t)slot;
+        int64_t t = r / K;
+        if (batched_hidden != NULL)
+            memcpy((char *)batched_hidden + slot * row_bytes,
+                   (const char *)hidden + t * row_bytes, (size_t)row_bytes);
+        if (batched_scales != NULL && scale_cols > 0)
+            memcpy(batched_scales + slot * scale_cols, scales + t * scale_cols,
+                   (size_t)scale_cols * sizeof(float));
+    }
+    for (int32_t e = 0; e < E_local; ++e)
+        expert_num_tokens[e] = (int32_t)(next[e] < M ? next[e] : M);
+    free(next);
+    return flags;
 }

@@ -446,9 +446,60 @@ def pin_quantize_properties(orc, seed=9):
     assert np.all(np.abs(deq - xb) <= bound)
 
 
+# -------------------------------------------------------- batched layout ---
+
+def pin_batched_golden(orc):
+    for c in load_golden()["batched"]:
+        emap = None if c["expert_map"] is None else np.array(c["expert_map"], np.int32)
+        r = orc.permute_batched(np.array(c["topk_ids"], np.int32), c["E"], c["M"],
+                                expert_map=emap, E_local=c["E_local"])
+        assert r["expert_num_tokens"].tolist() == c["expert_num_tokens"], c["name"]
+        assert r["inv_permuted_idx"].tolist() == c["inv_permuted_idx"], c["name"]
+        assert r["flags"] == c["flags"], c["name"]
+
+
+def pin_batched_brute_random(orc, n_cases=200, seed=10):
+    rng = np.random.default_rng(seed)
+    for _ in range(n_cases):
+        T = int(rng.integers(0, 12))
+        K = int(rng.integers(1, 4))
+        E = int(rng.integers(1, 6))
+        M = int(rng.integers(1, 6))  # small capacities: overflow is common
+        ids, emap, E_local = random_tiny_routing(rng, T, K, E, bool(rng.random() < 0.5), True)
+        res = orc.permute_batched(ids.astype(np.int32).reshape(T, K), E, M, expert_map=emap,
+                                  E_local=E_local)
+        ref = brute.permute_batched(ids.tolist(), E, M, expert_map=emap, E_local=E_local)
+        assert res["expert_num_tokens"].tolist() == ref["expert_num_tokens"]
+        assert res["inv_permuted_idx"].tolist() == ref["inv_permuted_idx"]
+        assert res["flags"] == ref["flags"]
+
+
+def pin_batched_vs_contiguous(orc, seed=11):
+    """With room for every row, slot = e*M + (p - offset[e]) where p is the
+    row's position in the contiguous layout, and each slot holds its token."""
+    rng = np.random.default_rng(seed)
+    T, K, E, H = 200, 6, 16, 24
+    ids, emap, E_local = random_tiny_routing(rng, T, K, E, True, False)
+    hidden = rng.integers(0, 65535, size=(T, H), dtype=np.uint16)
+    cont = orc.permute(ids.astype(np.int32), E, expert_map=emap, E_local=E_local)
+    M = int(np.diff(cont["offsets"]).max()) + 3
+    bat = orc.permute_batched(ids.astype(np.int32), E, M, expert_map=emap, E_local=E_local,
+                              hidden=hidden)
+    assert bat["flags"] == 0
+    assert np.array_equal(bat["expert_num_tokens"], np.diff(cont["offsets"]))
+    inv_c = cont["inv_permuted_idx"]
+    keys = local_keys(ids, E, emap, E_local)
+    want = np.where(inv_c >= 0, keys * M + (inv_c - cont["offsets"][np.maximum(keys, 0)]), -1)
+    assert np.array_equal(bat["inv_permuted_idx"], want)
+    slots = bat["inv_permuted_idx"][bat["inv_permuted_idx"] >= 0]
+    rows = np.flatnonzero(bat["inv_permuted_idx"] >= 0)
+    assert np.array_equal(bat["batched_hidden"][slots], hidden[rows // K])
+
+
 ALL_PINS = [pin_golden_routing, pin_golden_unpermute, pin_golden_rounding,
             pin_rounding_vs_torch, pin_brute_random, pin_exhaustive_tiny,
             pin_invariants, pin_closed_forms, pin_rows_copied,
             pin_unpermute_one_hot, pin_unpermute_bound, pin_flags,
             pin_e4m3_exhaustive, pin_e4m3_ties_and_neighbours,
-            pin_e4m3_vs_torch_and_saturation, pin_quantize_golden, pin_quantize_properties]
+            pin_e4m3_vs_torch_and_saturation, pin_quantize_golden, pin_quantize_properties,
+            pin_batched_golden, pin_batched_brute_random, pin_batched_vs_contiguous]

@@ -19,8 +19,8 @@ MUTANTS = {
     "unstable_order": ("for (int64_t r = 0; r < R; ++r) {\n        if (key[r] < 0) {",
                        "for (int64_t r = R - 1; r >= 0; --r) {\n        if (key[r] < 0) {"),
     "inclusive_offsets": ("cursor[e] = offsets[e];", "cursor[e] = offsets[e + 1] - (count[e] > 0);"),
-    "row_from_p_not_r": ("(const char *)hidden + t * row_bytes",
-                         "(const char *)hidden + (p / K) * row_bytes"),
+    "row_from_p_not_r": ("(char *)permuted_hidden + p * row_bytes,\n                   (const char *)hidden + t * row_bytes",
+                         "(char *)permuted_hidden + p * row_bytes,\n                   (const char *)hidden + (p / K) * row_bytes"),
     "map_minus_one_flagged": ("if (e == -1)\n        return -1;", ""),
     "tail_not_filled": ("permuted_idx[p] = -1;\n\n    free", "(void)p;\n\n    free"),
     "id_range_off_by_one": ("g >= (int64_t)E", "g > (int64_t)E"),
@@ -30,7 +30,10 @@ MUTANTS = {
     "truncate_not_round": ("kept += 1u;", "kept += 0u;"),
     "ties_away_from_zero": ("(dropped == 0x8000u && (kept & 1u))", "(dropped == 0x8000u)"),
     "subtract_term": ("acc = acc + prod;", "acc = acc - prod;"),
-    "scale_row_wrong_token": ("scales + t * scale_cols", "scales + (t / 2) * scale_cols"),
+    "scale_row_wrong_token": ("permuted_scales + p * scale_cols, scales + t * scale_cols",
+                              "permuted_scales + p * scale_cols, scales + (t / 2) * scale_cols"),
+    "batched_row_wrong_token": ("(char *)batched_hidden + slot * row_bytes,\n                   (const char *)hidden + t * row_bytes",
+                                "(char *)batched_hidden + slot * row_bytes,\n                   (const char *)hidden + (t ^ 1) * row_bytes"),
     "e4m3_ties_away": ("if (frac > 0.5 || (frac == 0.5 && ((long long)fl & 1)))",
                        "if (frac >= 0.5)"),
     "e4m3_truncate": ("double m8 = orc_round_half_even(t * 8.0);", "double m8 = (double)(long long)(t * 8.0);"),
@@ -39,6 +42,11 @@ MUTANTS = {
     "e4m3_subnormal_grid": ("double m = orc_round_half_even(a * 512.0);", "double m = orc_round_half_even(a * 256.0);"),
     "quant_wrong_max": ("float scale = amax > 0.0f ? amax / 448.0f : 1.0f;",
                         "float scale = amax > 0.0f ? amax / 240.0f : 1.0f;"),
+    "batched_capacity_off_by_one": ("        if (j >= M) {\n            inv_permuted_idx[r] = -1;",
+                                    "        if (j > M) {\n            inv_permuted_idx[r] = -1;"),
+    "batched_slot_stride": ("int64_t slot = (int64_t)e * M + j;", "int64_t slot = (int64_t)e * (M - 1) + j;"),
+    "batched_count_unclamped": ("expert_num_tokens[e] = (int32_t)(next[e] < M ? next[e] : M);",
+                                "expert_num_tokens[e] = (int32_t)next[e];"),
     "quant_zero_group_scale": ("float scale = amax > 0.0f ? amax / 448.0f : 1.0f;",
                                "float scale = amax > 0.0f ? amax / 448.0f : 0.0f;"),
 }
