@@ -218,6 +218,24 @@ class Setup:
         self.qbytes = quant_permute_bytes(self.T, self.wl.H, self.wl.K, self.wl.e_local,
                                           self.Tv, self.Nv)
 
+    def enable_batched(self, dev, M):
+        """Batched-layout outputs with capacity M per local expert."""
+        self.bM = M
+        self.bcounts = torch.empty(self.wl.e_local, dtype=torch.int32, device=dev)
+        self.bhidden = torch.empty(self.wl.e_local * M, self.wl.H, dtype=self.hidden.dtype,
+                                   device=dev)
+        self.bscales = None if self.scales is None else torch.empty(
+            self.wl.e_local * M, self.scales.shape[1], dtype=torch.float32, device=dev)
+        # same bytes as the contiguous permute minus the permuted_idx writes
+        self.bbytes = self.pbytes - self.T * self.wl.K * 4
+
+    def permute_batched(self):
+        self.mp.moe_permute_batched(self.hidden, self.ids, self.bcounts, self.inv, self.ws,
+                                    num_experts=self.wl.E, num_local_experts=self.wl.e_local,
+                                    max_rows_per_expert=self.bM, expert_map=self.emap,
+                                    hidden_scales=self.scales, batched_hidden_states=self.bhidden,
+                                    batched_scales=self.bscales)
+
     def permute_quant(self):
         self.mp.moe_permute_quant_fp8(self.qhidden, self.ids, self.offsets, self.pidx, self.inv,
                                       self.ws, self.qcodes, self.qscales, num_experts=self.wl.E,
@@ -307,7 +325,8 @@ def sweep(dev, peak, flush):
     replaying a CUDA graph of back-to-back calls (no Python launch cost);
     *_eager_us the same calls launched one by one from Python; at T = 1 also a
     single eager call after an L2 flush.  For the DeepSeek-V3 shape also
-    quantise-on-permute from bf16 rows (quant_fp8_permute_*)."""
+    quantise-on-permute from bf16 rows (quant_fp8_permute_*); for the Qwen3
+    shape also the batched layout with capacity M = T (batched_permute_*)."""
     rows = []
     for name, wl in WORKLOADS.items():
         if name == "tiny":
@@ -329,6 +348,13 @@ def sweep(dev, peak, flush):
                    "unpermute_frac": round(s0.ubytes / u_us / 1e3 / peak, 4),
                    "permute_eager_us": round(back_to_back_us([s.permute for s in sets], n), 2),
                    "unpermute_eager_us": round(back_to_back_us([s.unpermute for s in sets], n), 2)}
+            if name == "qwen3" and T >= 1024:
+                for st in sets:
+                    st.enable_batched(dev, T)
+                b_us = graph_us([st.permute_batched for st in sets], n_graph)
+                rec["batched_permute_us"] = round(b_us, 2)
+                rec["batched_permute_GBps"] = round(s0.bbytes / b_us / 1e3, 1)
+                rec["batched_permute_frac"] = round(s0.bbytes / b_us / 1e3 / peak, 4)
             if name == "dsv3":
                 for st in sets:
                     st.enable_quant(dev)

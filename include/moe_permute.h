@@ -81,6 +81,8 @@ typedef enum { MOE_INDEX_INT32 = 0, MOE_INDEX_INT64 = 1 } moe_index_t;
 #define MOE_FLAG_INV_OUT_OF_RANGE 4u  /* unpermute: inv index >= num_rows or < -1 */
 #define MOE_FLAG_BARRIER_TIMEOUT  8u  /* permute: a bounded grid-barrier wait gave up
                                          (outputs of that call are undefined) */
+#define MOE_FLAG_CAPACITY_OVERFLOW 16u /* batched permute: an expert got more rows than
+                                          its capacity; the extra rows were dropped */
 
 /* Limits checked on the host. */
 #define MOE_MAX_TOPK 32
@@ -165,6 +167,42 @@ MOE_API int moe_permute(const void *hidden_states, moe_dtype_t hidden_dtype,
                 int32_t *permuted_idx, int32_t *inv_permuted_idx,
                 void *workspace, size_t workspace_bytes,
                 moe_stream_t stream);
+
+/*
+ * moe_permute_batched: moe_permute into the batched activation layout, the
+ * second of the two layouts the modular MoE kernel's activation-format enum
+ * distinguishes ("[Kernels] MoE refactor" (vLLM PR #19636), description):
+ * one fixed-capacity block of rows per local expert instead of contiguous
+ * variable-length segments.
+ *
+ *  max_rows_per_expert  M >= 1, the capacity of each expert's block
+ *                       (E_L * M <= INT32_MAX).  M = num_tokens always fits
+ *                       when a token's K experts are distinct.
+ *  batched_hidden_states [E_L, M, H] of hidden_dtype, or NULL (metadata only).
+ *                       Slot e*M + j holds the j-th row (stable, r order)
+ *                       routed to local expert e; slots j >= expert_num_tokens[e]
+ *                       are not written.
+ *  batched_scales       [E_L, M, scale_cols] fp32 or NULL, as for moe_permute.
+ *  expert_num_tokens    [E_L] int32: min(rows routed to e, M).
+ *  inv_permuted_idx     [T*K] int32: r -> slot e*M + j, or -1 for a dropped
+ *                       row.  Rows beyond an expert's capacity are dropped too
+ *                       and raise MOE_FLAG_CAPACITY_OVERFLOW.  moe_unpermute
+ *                       with num_rows = E_L * M reduces the batched GEMM
+ *                       output back to tokens.
+ *  Inputs, dropped-row rules, workspace rules and errors are those of
+ *  moe_permute; T = 0 sets expert_num_tokens to 0 (other pointers may be NULL).
+ */
+MOE_API int moe_permute_batched(const void *hidden_states, moe_dtype_t hidden_dtype,
+                                const float *hidden_scales, int64_t scale_cols,
+                                const void *topk_ids, moe_index_t topk_ids_dtype,
+                                const int32_t *expert_map,
+                                int64_t num_tokens, int64_t hidden_size, int32_t topk,
+                                int32_t num_experts, int32_t num_local_experts,
+                                int64_t max_rows_per_expert,
+                                void *batched_hidden_states, float *batched_scales,
+                                int32_t *expert_num_tokens, int32_t *inv_permuted_idx,
+                                void *workspace, size_t workspace_bytes,
+                                moe_stream_t stream);
 
 /*
  * moe_permute_quant_fp8: moe_permute for bf16 activations that feed an fp8

@@ -14,7 +14,8 @@ from dataclasses import dataclass, field
 import torch
 
 from . import _binding as _b
-from ._binding import (MOE_FLAG_ID_OUT_OF_RANGE, MOE_FLAG_INV_OUT_OF_RANGE,  # noqa: F401
+from ._binding import (MOE_FLAG_BARRIER_TIMEOUT, MOE_FLAG_CAPACITY_OVERFLOW,  # noqa: F401
+                       MOE_FLAG_ID_OUT_OF_RANGE, MOE_FLAG_INV_OUT_OF_RANGE,
                        MOE_FLAG_MAP_OUT_OF_RANGE, MOE_MAX_LOCAL_EXPERTS, MOE_MAX_TOPK,
                        MoeError, library_path)
 
@@ -93,6 +94,32 @@ def moe_permute(hidden_states, topk_ids, expert_first_token_offset, permuted_idx
         _ptr(permuted_hidden_states), _ptr(permuted_scales),
         _ptr(expert_first_token_offset), _ptr(permuted_idx), _ptr(inv_permuted_idx),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def moe_permute_batched(hidden_states, topk_ids, expert_num_tokens, inv_permuted_idx, workspace,
+                        *, num_experts, max_rows_per_expert, num_local_experts=None,
+                        expert_map=None, hidden_scales=None, batched_hidden_states=None,
+                        batched_scales=None, stream=None) -> None:
+    """Permute into the batched layout (see include/moe_permute.h):
+    batched_hidden_states [E_local * M, H] (or [E_local, M, H]),
+    expert_num_tokens int32 [E_local], inv_permuted_idx int32 [T*K] holding
+    slots e*M + j."""
+    T, K = topk_ids.shape
+    if num_local_experts is None:
+        num_local_experts = num_experts
+    if hidden_states is not None:
+        H = hidden_states.shape[1]
+        dt = _DTYPES[hidden_states.dtype]
+    else:
+        H, dt = 1, _b.MOE_DTYPE_BF16
+    scale_cols = hidden_scales.shape[1] if hidden_scales is not None else 0
+    _b.check("moe_permute_batched", _b.lib().moe_permute_batched(
+        _ptr(hidden_states), dt, _ptr(hidden_scales), scale_cols,
+        _ptr(topk_ids), _INDEX[topk_ids.dtype], _ptr(expert_map),
+        T, H, K, num_experts, num_local_experts, int(max_rows_per_expert),
+        _ptr(batched_hidden_states), _ptr(batched_scales), _ptr(expert_num_tokens),
+        _ptr(inv_permuted_idx), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
 
 
 def moe_permute_quant_fp8(hidden_states, topk_ids, expert_first_token_offset, permuted_idx,

@@ -30,6 +30,8 @@ MOE_INDEX_INT64 = 1
 MOE_FLAG_ID_OUT_OF_RANGE = 1
 MOE_FLAG_MAP_OUT_OF_RANGE = 2
 MOE_FLAG_INV_OUT_OF_RANGE = 4
+MOE_FLAG_BARRIER_TIMEOUT = 8
+MOE_FLAG_CAPACITY_OVERFLOW = 16
 
 MOE_MAX_TOPK = 32
 MOE_MAX_LOCAL_EXPERTS = 1024
@@ -52,6 +54,9 @@ SIGNATURES = {
     "moe_unpermute": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I32, _P, _P, _P]),
     "moe_read_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
     "moe_clear_status": (ctypes.c_int, [_P, _P]),
+    "moe_permute_batched": (ctypes.c_int, [_P, ctypes.c_int, _P, _I64, _P, ctypes.c_int, _P,
+                                           _I64, _I64, _I32, _I32, _I32, _I64,
+                                           _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_quant_fp8": (ctypes.c_int, [_P, _P, ctypes.c_int, _P, _I64, _I64, _I32, _I32,
                                              _I32, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "moe_permute_noalloc": (ctypes.c_int, [_P, ctypes.c_int, _P, _I64, _P, ctypes.c_int, _P,

@@ -174,7 +174,8 @@ cudaError_t launch_fused(const IdT* ids, const int32_t* emap, int64_t T, int K, 
 template <typename IdT>
 cudaError_t launch_route(const IdT* ids, const int32_t* emap, int64_t T, int K, int E, int E_local,
                          int64_t* offsets, int32_t* pidx, int32_t* inv, WsHeader* hdr,
-                         const DeviceInfo* d, cudaStream_t s) {
+                         const DeviceInfo* d, cudaStream_t s, int64_t batch_capacity = 0,
+                         int32_t* expert_num_tokens = nullptr) {
   auto kern = k_route_coop<IdT>;
   const size_t smem = (static_cast<size_t>(kRouteWarps) * E_local + 4 * E_local + 1) * sizeof(int);
   cudaError_t err = allow_smem(kern, smem);
@@ -201,19 +202,34 @@ cudaError_t launch_route(const IdT* ids, const int32_t* emap, int64_t T, int K, 
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, ids, emap, T, K, E, E_local, offsets, pidx, inv, hdr,
-                            table);
+                            table, batch_capacity, expert_num_tokens);
 }
 
 template <typename VecT, int V>
 cudaError_t launch_gather(const void* hidden, int64_t row_bytes, const float* scales,
                           int64_t scale_cols, const int32_t* inv, int64_t T, int K, void* out,
-                          float* out_scales, cudaStream_t s) {
+                          float* out_scales, int64_t num_out_rows, cudaStream_t s) {
   const int64_t row_vecs = row_bytes / static_cast<int64_t>(sizeof(VecT));
   const int64_t blocks = ceil_div(row_items(T, row_vecs, V), kRowWarps);
   if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
   return launch(k_gather_rows<VecT, V>, static_cast<unsigned>(blocks), kRowThreads, 0, s,
                 static_cast<const VecT*>(hidden), row_vecs, scales, scale_cols, inv, T, K,
-                static_cast<VecT*>(out), out_scales);
+                static_cast<VecT*>(out), out_scales, num_out_rows);
+}
+
+// The row gather for any vector width: out rows are indexed by inv values in
+// [0, num_out_rows).
+cudaError_t launch_gather_any(size_t vb, const void* hidden, int64_t row_bytes,
+                              const float* scales, int64_t scale_cols, const int32_t* inv,
+                              int64_t T, int K, void* out, float* out_scales,
+                              int64_t num_out_rows, cudaStream_t s) {
+  switch (vb) {
+    case 16: return launch_gather<uint4, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, num_out_rows, s);
+    case 8: return launch_gather<uint2, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, num_out_rows, s);
+    case 4: return launch_gather<uint32_t, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, num_out_rows, s);
+    case 2: return launch_gather<uint16_t, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, num_out_rows, s);
+    default: return launch_gather<uint8_t, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, num_out_rows, s);
+  }
 }
 
 template <typename IdT>
@@ -236,13 +252,22 @@ cudaError_t permute_typed(const IdT* ids, const int32_t* emap, int64_t T, int K,
   }
   cudaError_t err = launch_route<IdT>(ids, emap, T, K, E, E_local, offsets, pidx, inv, hdr, d, s);
   if (err != cudaSuccess || out == nullptr) return err;
-  switch (vb) {
-    case 16: return launch_gather<uint4, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, s);
-    case 8: return launch_gather<uint2, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, s);
-    case 4: return launch_gather<uint32_t, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, s);
-    case 2: return launch_gather<uint16_t, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, s);
-    default: return launch_gather<uint8_t, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, s);
-  }
+  return launch_gather_any(vb, hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales,
+                           R, s);
+}
+
+template <typename IdT>
+cudaError_t permute_batched_typed(const IdT* ids, const int32_t* emap, int64_t T, int K, int E,
+                                  int E_local, int64_t M, const void* hidden, int64_t row_bytes,
+                                  const float* scales, int64_t scale_cols, void* out,
+                                  float* out_scales, int32_t* counts, int32_t* inv, void* ws,
+                                  const DeviceInfo* d, cudaStream_t s) {
+  cudaError_t err = launch_route<IdT>(ids, emap, T, K, E, E_local, nullptr, nullptr, inv,
+                                      static_cast<WsHeader*>(ws), d, s, M, counts);
+  if (err != cudaSuccess || out == nullptr) return err;
+  const size_t vb = vec_bytes(row_bytes, hidden, out);
+  return launch_gather_any(vb, hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales,
+                           static_cast<int64_t>(E_local) * M, s);
 }
 
 constexpr int kQuantV = 4;  // vectors of 8 bf16 per lane in one quantise item (8 groups)
@@ -260,7 +285,7 @@ cudaError_t permute_quant_typed(const IdT* ids, const int32_t* emap, int64_t T, 
   if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
   return launch(k_gather_quant_fp8<kQuantV>, static_cast<unsigned>(blocks), kRowThreads, 0, s,
                 static_cast<const uint4*>(hidden), row_vecs, static_cast<const int32_t*>(inv), T,
-                K, static_cast<uint2*>(codes), scales);
+                K, static_cast<uint2*>(codes), scales, T * K);
 }
 
 template <typename VecT, int KG, int V>
@@ -457,6 +482,67 @@ int moe_permute_quant_fp8(const void* hidden_states, const void* topk_ids,
                                        num_experts, num_local_experts, hidden_states, H,
                                        permuted_codes, permuted_scales, expert_first_token_offset,
                                        permuted_idx, inv_permuted_idx, workspace, d, s);
+  }
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_permute_batched(const void* hidden_states, moe_dtype_t hidden_dtype,
+                        const float* hidden_scales, int64_t scale_cols, const void* topk_ids,
+                        moe_index_t topk_ids_dtype, const int32_t* expert_map,
+                        int64_t num_tokens, int64_t hidden_size, int32_t topk,
+                        int32_t num_experts, int32_t num_local_experts,
+                        int64_t max_rows_per_expert, void* batched_hidden_states,
+                        float* batched_scales, int32_t* expert_num_tokens,
+                        int32_t* inv_permuted_idx, void* workspace, size_t workspace_bytes,
+                        moe_stream_t stream) {
+  const int eb = elem_bytes(hidden_dtype);
+  const int64_t T = num_tokens, H = hidden_size, M = max_rows_per_expert;
+  if (eb == 0 || T < 0 || H < 1 || topk < 1 || topk > MOE_MAX_TOPK || num_experts < 1 ||
+      num_local_experts < 1 || num_local_experts > num_experts ||
+      num_local_experts > MOE_MAX_LOCAL_EXPERTS || M < 1 || M > INT32_MAX / num_local_experts)
+    return MOE_ERR_INVALID_ARG;
+  if (expert_map == nullptr && num_local_experts != num_experts) return MOE_ERR_INVALID_ARG;
+  if (topk_ids_dtype != MOE_INDEX_INT32 && topk_ids_dtype != MOE_INDEX_INT64)
+    return MOE_ERR_INVALID_ARG;
+  if (T > INT32_MAX / topk || H > INT64_MAX / 16 / eb || scale_cols < 0) return MOE_ERR_INVALID_ARG;
+  if (expert_num_tokens == nullptr || !aligned(expert_num_tokens, 4)) return MOE_ERR_INVALID_ARG;
+  if (T > 0) {
+    const size_t id_bytes = topk_ids_dtype == MOE_INDEX_INT64 ? 8 : 4;
+    if (topk_ids == nullptr || !aligned(topk_ids, id_bytes)) return MOE_ERR_INVALID_ARG;
+    if (expert_map != nullptr && !aligned(expert_map, 4)) return MOE_ERR_INVALID_ARG;
+    if (inv_permuted_idx == nullptr || !aligned(inv_permuted_idx, 4)) return MOE_ERR_INVALID_ARG;
+    if (batched_hidden_states != nullptr && hidden_states == nullptr) return MOE_ERR_INVALID_ARG;
+    const bool with_scales = hidden_scales != nullptr || batched_scales != nullptr;
+    if (with_scales) {
+      if (hidden_scales == nullptr || batched_scales == nullptr || scale_cols < 1 ||
+          batched_hidden_states == nullptr || !aligned(hidden_scales, 4) ||
+          !aligned(batched_scales, 4))
+        return MOE_ERR_INVALID_ARG;
+    } else if (scale_cols != 0) {
+      return MOE_ERR_INVALID_ARG;
+    }
+    if (workspace == nullptr || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < workspace_bytes_for(T, topk, num_experts))
+      return MOE_ERR_WORKSPACE_TOO_SMALL;
+  }
+  const DeviceInfo* d = current_device();
+  if (!is_supported(d)) return MOE_ERR_UNSUPPORTED_DEVICE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (T == 0) {
+    err = cudaMemsetAsync(expert_num_tokens, 0, sizeof(int32_t) * num_local_experts, s);
+  } else if (topk_ids_dtype == MOE_INDEX_INT32) {
+    err = permute_batched_typed<int32_t>(static_cast<const int32_t*>(topk_ids), expert_map, T,
+                                         topk, num_experts, num_local_experts, M, hidden_states,
+                                         H * eb, hidden_scales, scale_cols, batched_hidden_states,
+                                         batched_scales, expert_num_tokens, inv_permuted_idx,
+                                         workspace, d, s);
+  } else {
+    err = permute_batched_typed<int64_t>(static_cast<const int64_t*>(topk_ids), expert_map, T,
+                                         topk, num_experts, num_local_experts, M, hidden_states,
+                                         H * eb, hidden_scales, scale_cols, batched_hidden_states,
+                                         batched_scales, expert_num_tokens, inv_permuted_idx,
+                                         workspace, d, s);
   }
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

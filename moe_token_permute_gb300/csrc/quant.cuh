@@ -29,7 +29,8 @@ template <int V>
 __global__ void __launch_bounds__(256)
 k_gather_quant_fp8(const uint4* __restrict__ hidden, int64_t row_vecs,
                    const int32_t* __restrict__ inv_permuted_idx, int64_t T, int K,
-                   uint2* __restrict__ out_codes, float* __restrict__ out_scales) {
+                   uint2* __restrict__ out_codes, float* __restrict__ out_scales,
+                   int64_t num_out_rows) {
   constexpr int64_t kChunk = 32 * V;  // vectors of 8 values per item
   const int lane = threadIdx.x & 31;
   const int64_t n_chunks = (row_vecs + kChunk - 1) / kChunk;
@@ -49,7 +50,7 @@ k_gather_quant_fp8(const uint4* __restrict__ hidden, int64_t row_vecs,
   // own dependency wait); the positions come from the routing grid.
   pdl_wait();
   int p = lane < K ? __ldcg(inv_permuted_idx + t * K + lane) : -1;
-  if (p >= T * K) p = -1;  // only a routing grid that gave up leaves such values
+  if (p >= num_out_rows) p = -1;  // only a routing grid that gave up leaves such values
   const unsigned valid = __ballot_sync(kFullMask, p >= 0);
   if (valid == 0u) return;
 

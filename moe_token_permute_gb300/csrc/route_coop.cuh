@@ -84,15 +84,38 @@ __device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned gen) {
   return s_ok != 0;
 }
 
+// Final position of a kept row whose contiguous position is p.  Contiguous
+// layout: p itself (and permuted_idx[p] = r).  Batched layout: slot
+// e*M + (p - first[e]), or -1 when the expert's capacity M is exceeded.
+__device__ __forceinline__ int place_row(int p, int e, int64_t r, int64_t M, const int* first,
+                                         int32_t* __restrict__ permuted_idx,
+                                         WsHeader* __restrict__ hdr) {
+  if (M == 0) {
+    permuted_idx[p] = static_cast<int32_t>(r);
+    return p;
+  }
+  const int64_t j = p - first[e];
+  if (j >= M) {
+    atomicOr(&hdr->status, MOE_FLAG_CAPACITY_OVERFLOW);
+    return -1;
+  }
+  return static_cast<int>(static_cast<int64_t>(e) * M + j);
+}
+
 // Shared memory: s_base [E_local + 1] | s_run [E_local] | s_tot [E_local] |
 //                s_bef [E_local] | cnt [kRouteWarps][E_local]
+// Batched layout (M > 0): instead of the contiguous segments, rows of local
+// expert e go to slots e*M + j, j = the row's stable rank inside the expert;
+// rows with j >= M are dropped (MOE_FLAG_CAPACITY_OVERFLOW).  Block 0 writes
+// expert_num_tokens[e] = min(rows of e, M); offsets and permuted_idx are not
+// used.
 template <typename IdT>
 __global__ void __launch_bounds__(kRouteThreads, 4)
 k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
              int64_t T, int K, int E, int E_local,
              int64_t* __restrict__ offsets, int32_t* __restrict__ permuted_idx,
              int32_t* __restrict__ inv_permuted_idx, WsHeader* __restrict__ hdr,
-             int* __restrict__ table) {
+             int* __restrict__ table, int64_t M, int32_t* __restrict__ expert_num_tokens) {
   extern __shared__ int smem[];
   __shared__ int s_warp[32];
   int* s_base = smem;                 // [E_local + 1]
@@ -204,20 +227,27 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
       const int e = threadIdx.x * kPer + u;
       if (e < E_local) {
         s_base[e] = run + s_bef[e];
-        if (b == 0) offsets[e] = run;
+        s_tot[e] = run;  // from here on: the expert's first contiguous position
+        if (b == 0) {
+          if (M > 0)
+            expert_num_tokens[e] = static_cast<int32_t>(min(static_cast<int64_t>(tot[u]), M));
+          else
+            offsets[e] = run;
+        }
       }
       run += tot[u];
     }
     if (threadIdx.x == 0) {
       s_base[E_local] = n_valid;
-      if (b == 0) offsets[E_local] = n_valid;
+      if (b == 0 && M == 0) offsets[E_local] = n_valid;
     }
   }
   __syncthreads();
   // Tail of permuted_idx: positions [N_valid, R) hold -1 (spread over blocks).
-  for (int64_t p = s_base[E_local] + static_cast<int64_t>(b) * blockDim.x + threadIdx.x; p < R;
-       p += static_cast<int64_t>(B) * blockDim.x)
-    permuted_idx[p] = -1;
+  if (M == 0)
+    for (int64_t p = s_base[E_local] + static_cast<int64_t>(b) * blockDim.x + threadIdx.x;
+         p < R; p += static_cast<int64_t>(B) * blockDim.x)
+      permuted_idx[p] = -1;
 
   // Phase 4: positions.
   if (one_round) {
@@ -229,7 +259,7 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
         int p = -1;
         if (e >= 0) {
           p = s_base[e] + cnt[warp * E_local + e] + rank[j];
-          permuted_idx[p] = static_cast<int32_t>(r);
+          p = place_row(p, e, r, M, s_tot, permuted_idx, hdr);
         }
         inv_permuted_idx[r] = p;
       }
@@ -266,7 +296,7 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
         int p = -1;
         if (e >= 0) {
           p = s_base[e] + cnt[warp * E_local + e] + rank[j];
-          permuted_idx[p] = static_cast<int32_t>(r);
+          p = place_row(p, e, r, M, s_tot, permuted_idx, hdr);
         }
         inv_permuted_idx[r] = p;
       }

@@ -84,7 +84,8 @@ __global__ void __launch_bounds__(kRowThreads)
 k_gather_rows(const VecT* __restrict__ hidden, int64_t row_vecs,
               const float* __restrict__ scales, int64_t scale_cols,
               const int32_t* __restrict__ inv_permuted_idx, int64_t T, int K,
-              VecT* __restrict__ permuted_hidden, float* __restrict__ permuted_scales) {
+              VecT* __restrict__ permuted_hidden, float* __restrict__ permuted_scales,
+              int64_t num_out_rows) {
   constexpr int64_t kChunk = 32 * V;
   const int lane = threadIdx.x & 31;
   const int64_t n_chunks = (row_vecs + kChunk - 1) / kChunk;
@@ -96,9 +97,9 @@ k_gather_rows(const VecT* __restrict__ hidden, int64_t row_vecs,
   load_chunk<VecT, V>(hidden + t * row_vecs, c0, row_vecs, v);
   pdl_wait();
   int p = lane < K ? __ldcg(inv_permuted_idx + t * K + lane) : -1;
-  // Positions outside [0, T*K) can only come from a routing grid that gave up
-  // (status MOE_FLAG_BARRIER_TIMEOUT); never store through them.
-  if (p >= T * K) p = -1;
+  // Positions outside [0, num_out_rows) can only come from a routing grid that
+  // gave up (status MOE_FLAG_BARRIER_TIMEOUT); never store through them.
+  if (p >= num_out_rows) p = -1;
   const unsigned valid = __ballot_sync(kFullMask, p >= 0);
   if (valid == 0u) return;  // every row of this token was dropped
   store_chunk<VecT, V>(v, permuted_hidden, c0, row_vecs, p, valid);
