@@ -144,6 +144,22 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- helpers ---
+def max_over_ranks(x_ms, dist, device):
+    """The slowest rank's time (no-op with one process): every rank runs the
+    same step on its own token batch, and the job is as fast as its slowest."""
+    if dist is None:
+        return x_ms
+    t = torch.tensor([x_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(world, bytes_per_rank_step, ms_per_step):
+    """Whole-job throughput: each of `world` ranks moves bytes_per_rank_step
+    per step, in the slowest rank's step time."""
+    return world * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -511,13 +527,9 @@ def main():
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    total_ms = start.elapsed_time(end)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(start.elapsed_time(end), dist, dev)
     ms_per_step = total_ms / n
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    value = job_gbs(world, step_bytes, ms_per_step)
 
     # Second pass over the same K steps with events around each call: the
     # per-op split and the duration of the dominant kernel (k_unpermute, one
@@ -564,12 +576,8 @@ def main():
         e2e_step()
     b.record()
     torch.cuda.synchronize()
-    e2e_ms = a.elapsed_time(b) / n_e2e
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(a.elapsed_time(b) / n_e2e, dist, dev)
+    e2e_value = job_gbs(world, step_bytes, e2e_ms)
 
     line = None
     if rank == 0:
