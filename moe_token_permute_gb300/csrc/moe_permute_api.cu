@@ -28,6 +28,7 @@
 #include "rows.cuh"
 #include "route_coop.cuh"
 #include "quant.cuh"
+#include "gather_tma.cuh"
 
 namespace moe {
 namespace {
@@ -40,6 +41,7 @@ struct DeviceInfo {
   int cc_minor = 0;
   int sm_count = 0;
   int max_smem_optin = 0;
+  int max_smem_per_sm = 0;
 };
 
 std::mutex g_dev_mutex;
@@ -56,7 +58,9 @@ const DeviceInfo* current_device() {
         cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
-            cudaSuccess)
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&d.max_smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                               dev) != cudaSuccess)
       return nullptr;
     d.ready = true;
   }
@@ -217,12 +221,53 @@ cudaError_t launch_gather(const void* hidden, int64_t row_bytes, const float* sc
                 static_cast<VecT*>(out), out_scales, num_out_rows);
 }
 
+// Geometry of the bulk-copy gather for one row size.
+struct TmaGeometry {
+  int64_t chunk, pitch, grid;
+  size_t smem;
+  int64_t prefetch_bytes;  // source bytes the whole grid loads before routing ends
+};
+
+TmaGeometry tma_geometry(int64_t row_bytes, int64_t T, const DeviceInfo* d) {
+  TmaGeometry g;
+  g.chunk = std::min<int64_t>(row_bytes, kTmaChunkBytes);
+  g.pitch = (g.chunk + 127) / 128 * 128;
+  g.smem = static_cast<size_t>(kTmaWarps) * kTmaStages * (g.pitch + sizeof(uint64_t));
+  const int64_t items = T * ceil_div(row_bytes, g.chunk);
+  const int64_t per_sm = std::max<int64_t>(
+      1, std::min<int64_t>(16, d->max_smem_per_sm / static_cast<int64_t>(g.smem + 1024)));
+  g.grid = std::max<int64_t>(1, std::min(ceil_div(items, kTmaWarps), per_sm * d->sm_count));
+  g.prefetch_bytes = g.grid * kTmaWarps * kTmaStages * g.chunk;
+  return g;
+}
+
+// Bulk-copy gather (16-byte aligned rows): a persistent grid of warps, each
+// with kTmaStages shared-memory stages of up to kTmaChunkBytes.
+cudaError_t launch_gather_tma(const void* hidden, int64_t row_bytes, const float* scales,
+                              int64_t scale_cols, const int32_t* inv, int64_t T, int K,
+                              void* out, float* out_scales, int64_t num_out_rows,
+                              unsigned* status, const DeviceInfo* d, cudaStream_t s) {
+  const TmaGeometry g = tma_geometry(row_bytes, T, d);
+  cudaError_t err = allow_smem(k_gather_rows_tma, g.smem);
+  if (err != cudaSuccess) return err;
+  return launch(k_gather_rows_tma, static_cast<unsigned>(g.grid), kTmaThreads, g.smem, s,
+                static_cast<const char*>(hidden), row_bytes, g.chunk, g.pitch, scales, scale_cols,
+                inv, T, K, static_cast<char*>(out), out_scales, num_out_rows, status);
+}
+
 // The row gather for any vector width: out rows are indexed by inv values in
-// [0, num_out_rows).
+// [0, num_out_rows).  16-byte aligned rows go through the bulk-copy engine
+// when most of the source rows fit its prefetch (it then loads them while the
+// routing grid runs); larger batches keep more loads in flight with the
+// register gather.
 cudaError_t launch_gather_any(size_t vb, const void* hidden, int64_t row_bytes,
                               const float* scales, int64_t scale_cols, const int32_t* inv,
                               int64_t T, int K, void* out, float* out_scales,
-                              int64_t num_out_rows, cudaStream_t s) {
+                              int64_t num_out_rows, unsigned* status, const DeviceInfo* d,
+                              cudaStream_t s) {
+  if (vb == 16 && 2 * T * row_bytes <= 3 * tma_geometry(row_bytes, T, d).prefetch_bytes)
+    return launch_gather_tma(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales,
+                             num_out_rows, status, d, s);
   switch (vb) {
     case 16: return launch_gather<uint4, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, num_out_rows, s);
     case 8: return launch_gather<uint2, kGatherV>(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales, num_out_rows, s);
@@ -253,7 +298,7 @@ cudaError_t permute_typed(const IdT* ids, const int32_t* emap, int64_t T, int K,
   cudaError_t err = launch_route<IdT>(ids, emap, T, K, E, E_local, offsets, pidx, inv, hdr, d, s);
   if (err != cudaSuccess || out == nullptr) return err;
   return launch_gather_any(vb, hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales,
-                           R, s);
+                           R, &hdr->status, d, s);
 }
 
 template <typename IdT>
@@ -267,7 +312,8 @@ cudaError_t permute_batched_typed(const IdT* ids, const int32_t* emap, int64_t T
   if (err != cudaSuccess || out == nullptr) return err;
   const size_t vb = vec_bytes(row_bytes, hidden, out);
   return launch_gather_any(vb, hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales,
-                           static_cast<int64_t>(E_local) * M, s);
+                           static_cast<int64_t>(E_local) * M,
+                           &static_cast<WsHeader*>(ws)->status, d, s);
 }
 
 constexpr int kQuantV = 4;  // vectors of 8 bf16 per lane in one quantise item (8 groups)
