@@ -37,6 +37,9 @@ from moe_token_permute_gb300.workloads import WORKLOADS, make_inputs  # noqa: E4
 
 METRIC = "permute/unpermute HBM GB/s (% of GB300 peak) and µs/call vs token count"
 HEADLINE = ("mixtral", 16384)
+WORKLOAD_NAMES = {"mixtral": "mixtral-8x7b-moe-layer", "qwen3": "qwen3-30b-a3b-moe-layer",
+                  "dsv2lite": "deepseek-v2-lite-moe-layer-expert-map",
+                  "dsv3": "deepseek-v3-moe-layer", "tiny": "tiny-moe-layer"}
 FALLBACK_HBM_GBS = 6800.0
 CSRC = os.path.join(ROOT, "moe_token_permute_gb300", "csrc")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
@@ -473,6 +476,11 @@ def main():
     ap.add_argument("--impl", default="own", choices=["own", "reference"])
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default=HEADLINE[0], choices=sorted(WORKLOADS),
+                    help="layer shape of the timed step (default: the headline)")
+    ap.add_argument("--tokens", type=int, default=HEADLINE[1], help="tokens per step")
+    ap.add_argument("--quant", action="store_true",
+                    help="permute bf16 rows with quantise-on-permute (fp8 e4m3 out)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -496,15 +504,25 @@ def main():
         raise SystemExit("this GPU is not an sm_103 device")
 
     peak, peak_kind = measured_peak()
-    name, T = HEADLINE
+    name, T = args.workload, args.tokens
     sets = [Setup(name, T, seed=rank * 2 + i, dev=dev) for i in range(2)]
     s0 = sets[0]
-    step_bytes = s0.pbytes + s0.ubytes
-    launches_per_step = s0.launches_per_permute() + 1
+    if args.quant:
+        for st in sets:
+            st.enable_quant(dev)
+    perm_bytes = s0.qbytes if args.quant else s0.pbytes
+    step_bytes = perm_bytes + s0.ubytes
+    launches_per_step = (2 if args.quant else s0.launches_per_permute()) + 1
+
+    def do_permute(s):
+        if args.quant:
+            s.permute_quant()
+        else:
+            s.permute()
 
     def step(i):
         s = sets[i % 2]
-        s.permute()
+        do_permute(s)
         s.unpermute()
 
     for i in range(args.warmup):
@@ -538,7 +556,7 @@ def main():
     for i in range(n):
         s = sets[i % 2]
         ev[i][0].record()
-        s.permute()
+        do_permute(s)
         ev[i][1].record()
         s.unpermute()
         ev[i][2].record()
@@ -547,7 +565,8 @@ def main():
     unp_us = 1e3 * sum(e[1].elapsed_time(e[2]) for e in ev) / n
 
     # end to end: pinned host inputs in, result out, every step
-    h_hidden = s0.hidden.cpu().pin_memory()
+    d_hidden = s0.qhidden if args.quant else s0.hidden
+    h_hidden = d_hidden.cpu().pin_memory()
     h_ids = s0.ids.cpu().pin_memory()
     h_w = s0.w.cpu().pin_memory()
     h_rows = s0.rows.cpu().pin_memory()
@@ -557,11 +576,11 @@ def main():
     d2h = h_out.numel() * h_out.element_size() + h_off.numel() * h_off.element_size()
 
     def e2e_step():
-        s0.hidden.copy_(h_hidden, non_blocking=True)
+        d_hidden.copy_(h_hidden, non_blocking=True)
         s0.ids.copy_(h_ids, non_blocking=True)
         s0.w.copy_(h_w, non_blocking=True)
         s0.rows.copy_(h_rows, non_blocking=True)
-        s0.permute()
+        do_permute(s0)
         s0.unpermute()
         h_out.copy_(s0.out, non_blocking=True)
         h_off.copy_(s0.offsets, non_blocking=True)
@@ -587,17 +606,22 @@ def main():
             "steps": n, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": "mixtral-8x7b-moe-layer", "T": T, "H": s0.wl.H, "E": s0.wl.E,
-                       "K": s0.wl.K, "routing": "uniform distinct top-2",
+            "config": {"workload": WORKLOAD_NAMES[name] + ("-quant-fp8" if args.quant else ""),
+                       "T": T, "H": s0.wl.H, "E": s0.wl.E, "E_local": s0.wl.e_local,
+                       "K": s0.wl.K,
+                       "routing": s0.wl.routing + (f" s={s0.wl.zipf_s}" if s0.wl.zipf_s else ""),
                        "parallelism": f"replicas x{world} (token batches, no collective)",
-                       "l2": f"inputs larger than L2: {step_bytes / 1e6:.0f} MB moved per step, "
-                             "two input sets alternate"},
+                       "l2": (f"inputs larger than L2: {step_bytes / 1e6:.0f} MB moved per step, "
+                              "two input sets alternate") if step_bytes > L2_BYTES else
+                             f"{step_bytes / 1e6:.0f} MB per step, two input sets alternate "
+                             "(together within L2)"},
             "frac_of_peak": round(value / world / peak, 4),
             "peak_GBps": peak, "peak_kind": peak_kind,
             "bytes_per_step": step_bytes,
-            "permute": {"us_per_call": round(perm_us, 2), "GBps": round(s0.pbytes / perm_us / 1e3, 1),
-                        "frac": round(s0.pbytes / perm_us / 1e3 / peak, 4), "bytes": s0.pbytes,
-                        "launches": s0.launches_per_permute()},
+            "permute": {"us_per_call": round(perm_us, 2), "GBps": round(perm_bytes / perm_us / 1e3, 1),
+                        "frac": round(perm_bytes / perm_us / 1e3 / peak, 4), "bytes": perm_bytes,
+                        "launches": launches_per_step - 1,
+                        "op": "moe_permute_quant_fp8" if args.quant else "moe_permute"},
             "unpermute": {"us_per_call": round(unp_us, 2), "GBps": round(unp_gbs, 1),
                           "frac": round(unp_gbs / peak, 4), "bytes": s0.ubytes, "launches": 1},
             "roofline": {"kernel": "k_unpermute", "bound": "hbm", "achieved": round(unp_gbs, 1),
