@@ -270,9 +270,9 @@ class Setup:
         self.mp.moe_unpermute(self.rows, self.w, self.inv, self.out, workspace=self.ws)
 
     def launches_per_permute(self):
-        """Kernels one moe_permute call launches: one up to 1024 expanded rows,
+        """Kernels one moe_permute call launches: one up to 2048 expanded rows,
         else the routing grid plus the gather."""
-        return 1 if self.T * self.wl.K <= 1024 else 2
+        return 1 if self.T * self.wl.K <= 2048 else 2
 
     def footprint(self):
         ts = [self.hidden, self.scales, self.ids, self.w, self.rows, self.emap, self.offsets,

@@ -123,7 +123,7 @@ size_t workspace_bytes_for(int64_t max_tokens, int32_t topk, int32_t num_experts
 
 constexpr int kFusedV = 4;   // vectors per lane in one gather chunk (fused kernel)
 constexpr int kGatherV = 8;  // same, gather kernel of the large-batch path
-constexpr int64_t kFusedMaxRows = 1024;  // R above this: the cooperative kernel
+constexpr int64_t kFusedMaxRows = 2048;  // R above this: routing grid + gather
 
 // (token, chunk) work items of a row kernel.
 int64_t row_items(int64_t T, int64_t row_vecs, int V) {

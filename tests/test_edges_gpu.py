@@ -15,7 +15,7 @@ from gpu_util import (alloc_outputs, assert_metadata_equal, assert_rows_equal_fu
 
 pytestmark = pytest.mark.gpu
 
-CHUNK = 8192  # expanded rows handled by one routing block (single-launch limit)
+CHUNK = 8192  # sizes around the rows one block ranks in one pass (single launch: <= 2048 rows)
 
 
 def custom_inputs(T, K, E, H, dtype=torch.bfloat16, E_local=None, emap=None, ids=None,
@@ -74,7 +74,8 @@ def test_zero_tokens():
                      torch.empty(0, dtype=torch.int32, device="cuda"), out)
 
 
-@pytest.mark.parametrize("T,K", [(CHUNK, 1), (CHUNK + 1, 1), (1024, 8), (1025, 8),
+@pytest.mark.parametrize("T,K", [(2048, 1), (2049, 1), (256, 8), (257, 8),
+                                 (CHUNK, 1), (CHUNK + 1, 1), (1024, 8), (1025, 8),
                                  (3 * CHUNK // 2 + 3, 2), (5 * CHUNK + 17, 1)])
 def test_single_and_multi_launch_boundary(T, K):
     check_case(custom_inputs(T, K, 64, 96, seed=T))
