@@ -79,8 +79,9 @@ typedef enum { MOE_INDEX_INT32 = 0, MOE_INDEX_INT64 = 1 } moe_index_t;
 #define MOE_FLAG_ID_OUT_OF_RANGE  1u  /* a topk id outside [0, num_experts) */
 #define MOE_FLAG_MAP_OUT_OF_RANGE 2u  /* expert_map value not -1 and outside [0, num_local_experts) */
 #define MOE_FLAG_INV_OUT_OF_RANGE 4u  /* unpermute: inv index >= num_rows or < -1 */
-#define MOE_FLAG_BARRIER_TIMEOUT  8u  /* permute: a bounded grid-barrier wait gave up
-                                         (outputs of that call are undefined) */
+#define MOE_FLAG_BARRIER_TIMEOUT  8u  /* permute: a bounded wait for another block's
+                                         histogram gave up (outputs of that call are
+                                         undefined; re-initialise the workspace) */
 #define MOE_FLAG_CAPACITY_OVERFLOW 16u /* batched permute: an expert got more rows than
                                           its capacity; the extra rows were dropped */
 
@@ -112,10 +113,12 @@ MOE_API size_t moe_permute_workspace_size(int64_t max_tokens, int32_t topk,
                                   int32_t num_experts);
 
 /*
- * moe_permute_workspace_init: zero the workspace's control words (grid
- * barrier and status).  Call once after allocating the workspace (async on `stream`); every
- * later call leaves the workspace ready for the next one.  `workspace` must be
- * 256-byte aligned and at least moe_permute_workspace_size(...) bytes.
+ * moe_permute_workspace_init: zero the first `workspace_bytes` bytes of the
+ * workspace (status word, call counter, histogram table).  Call once after
+ * allocating the workspace (async on `stream`), with the size that was
+ * allocated; every later call leaves the workspace ready for the next one.
+ * `workspace` must be 256-byte aligned and at least
+ * moe_permute_workspace_size(...) bytes.
  */
 MOE_API int moe_permute_workspace_init(void *workspace, size_t workspace_bytes,
                                moe_stream_t stream);
@@ -280,7 +283,7 @@ MOE_API int moe_clear_status(void *workspace, moe_stream_t stream);
  * MOE_NOALLOC_SCRATCH_BYTES inside this library: every GPU that loads the
  * library holds it until the process exits.  Nothing is allocated or freed.
  *  - The first call on a device looks up that array's device address and
- *    zeroes its control words (stream-ordered on `stream`).  Make that first
+ *    zeroes it (stream-ordered on `stream`).  Make that first
  *    call before capturing any stream into a CUDA graph.
  *  - Every call on a device shares the one array, which keeps the last call's
  *    contents.  Calls that may overlap on the GPU (two streams, or parallel

@@ -16,8 +16,8 @@ constexpr unsigned kFullMask = 0xffffffffu;
 struct WsHeader {
   unsigned reserved0;
   unsigned status;  // OR of MOE_FLAG_* bits
-  unsigned arrive;  // grid barrier: blocks arrived (the last one resets it)
-  unsigned gen;     // grid barrier: generation, bumped once per barrier
+  unsigned table_hi;  // histogram-table entries the last routing grid wrote or left
+  unsigned gen;       // routing calls so far (mod 2^32): the source of each call's table tag
   unsigned reserved[60];
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");

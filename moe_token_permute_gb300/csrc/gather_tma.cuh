@@ -14,7 +14,12 @@
 // and keeps kTmaStages of them in flight.  Its first kTmaStages loads are
 // issued before it waits for the routing grid (the caller's rows are complete
 // by then: this grid only starts once the routing grid has passed its own
-// dependency wait), so they overlap the routing.
+// dependency wait), so they overlap the routing.  They go out one at a time,
+// each after the previous one has landed: with every warp's stages requested
+// at once (tens of MB) the memory system's queues fill, and the routing
+// grid's few small reads of its histogram table wait behind them for the
+// whole drain (measured: 4-5 us instead of 1 us; the chained prefetch is
+// 5-10% faster end to end on batches of about the prefetch capacity).
 //
 // Requirements (checked on the host): row pitch, chunk offsets and both base
 // pointers are multiples of 16 bytes.
@@ -136,7 +141,11 @@ k_gather_rows_tma(const char* __restrict__ hidden, int64_t row_bytes, int64_t ch
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     for (int s = 0; s < kTmaStages; ++s) {
       const int64_t item = gw + s * n_gw;
-      if (item < n_items) issue_load(item, s);
+      if (item >= n_items) break;
+      // A wait that gives up here is not acted on: the main loop's bounded
+      // wait for the same stage flags it.
+      if (s > 0) (void)mbar_wait_bounded(&bars[s - 1], 0u);
+      issue_load(item, s);
     }
   }
   __syncwarp();

@@ -190,8 +190,11 @@ cudaError_t launch_route(const IdT* ids, const int32_t* emap, int64_t T, int K, 
   // free for the gather blocks that start while routing runs.
   const int64_t tokens_per_round = std::max<int64_t>(1, kRouteRoundRows / K);
   int64_t B = std::min<int64_t>(ceil_div(T, tokens_per_round), d->sm_count);
+  // A table entry holds a block's rows of one expert in 24 bits.
+  B = std::max(B, ceil_div(T, static_cast<int64_t>(kCountMask) / K));
   B = std::max<int64_t>(1, std::min(B, kCoopMaxBlocks));
-  int* table = reinterpret_cast<int*>(reinterpret_cast<char*>(hdr) + kWsHeaderBytes);
+  if (ceil_div(T, B) * K > static_cast<int64_t>(kCountMask)) return cudaErrorInvalidConfiguration;
+  unsigned* table = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(hdr) + kWsHeaderBytes);
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3(static_cast<unsigned>(B));
@@ -408,7 +411,7 @@ int moe_permute_workspace_init(void* workspace, size_t workspace_bytes, moe_stre
   if (workspace == nullptr || !aligned(workspace, 256) || workspace_bytes < kWsHeaderBytes)
     return MOE_ERR_INVALID_ARG;
   if (!is_supported(current_device())) return MOE_ERR_UNSUPPORTED_DEVICE;
-  if (cudaMemsetAsync(workspace, 0, kWsHeaderBytes, reinterpret_cast<cudaStream_t>(stream)) !=
+  if (cudaMemsetAsync(workspace, 0, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
@@ -681,7 +684,7 @@ extern "C" int moe_permute_noalloc(const void* hidden_states, moe_dtype_t hidden
         cudaGetLastError();
         return MOE_ERR_CUDA;
       }
-      if (cudaMemsetAsync(ptr, 0, kWsHeaderBytes, reinterpret_cast<cudaStream_t>(stream)) !=
+      if (cudaMemsetAsync(ptr, 0, MOE_NOALLOC_SCRATCH_BYTES, reinterpret_cast<cudaStream_t>(stream)) !=
           cudaSuccess)
         return MOE_ERR_CUDA;
       g_noalloc_ptr[dev] = ptr;

@@ -1,5 +1,6 @@
 // route_coop.cuh -- routing metadata of moe_permute for large batches: one
-// cooperatively launched grid with a single grid barrier.
+// cooperatively launched grid whose blocks exchange per-expert histograms
+// through a tagged table instead of a grid barrier.
 //
 // vLLM PR #14568 ("permute/unpermute kernel for moe optimization",
 // description): expand each token to its K rows and order the rows by expert
@@ -8,21 +9,32 @@
 //
 // Block b owns the contiguous tokens [b*tpb, (b+1)*tpb), i.e. the contiguous
 // rows [r0, r1).  Phases:
-//   1. histogram of the block's rows -> table[b][e] (workspace).  When the
-//      block's rows fit one round (kRouteRoundRows), the stable in-block ranks
-//      are computed in the same pass and kept in registers;
-//   2. one grid barrier (every block is resident: cooperative launch);
-//   3. every block reads the whole [B][E_local] table with 16-byte loads:
-//      offsets (block 0 writes them) and its bases
-//      base[e] = offset[e] + sum_{b'<b} table[b'][e];
-//   4. positions p = base[e] + (rows of expert e before r in the block) ->
+//   1. histogram of the block's rows -> row b of the table (workspace), each
+//      entry tagged with this call's tag.  When the block's rows fit one
+//      round (kRouteRoundRows), the stable in-block ranks are computed in the
+//      same pass and kept in registers;
+//   2. every block reads the whole [B][E_local] table with 16-byte loads,
+//      re-reading entries that do not carry this call's tag yet (every block
+//      is resident: cooperative launch), and forms the offsets (block 0 writes
+//      them) and its bases base[e] = offset[e] + sum_{b'<b} table[b'][e];
+//   3. positions p = base[e] + (rows of expert e before r in the block) ->
 //      permuted_idx, inv_permuted_idx (in rounds when the block has more rows).
+// A tagged entry is its own completion flag, so no block waits on a counter,
+// a fence or another block's arrival: each waits only until the rows it reads
+// have landed.
+// Tags: entry = tag << 24 | count, tag = 0x80 | (gen & 0x7f), gen a word of
+// the workspace header that block 0 advances by one per call (after it has
+// seen every row, i.e. after every block has read gen).  Block 0 also zeroes
+// the entries past this call's extent that an earlier call left.  So while a
+// call runs, every entry holds zero, the previous call's tag or this call's:
+// a stale entry can never pass for a fresh one.
 // The kernel lets the row-gather kernel that follows launch as soon as it
 // starts: those blocks load their source rows while routing runs and wait for
 // this grid before they read inv_permuted_idx.
-// The barrier wait is bounded (2^24 polls or 2 s): on timeout the status word
-// gets MOE_FLAG_BARRIER_TIMEOUT and the kernel returns (outputs undefined; the
-// gather that follows never stores through an out-of-range position).
+// Every wait for a table entry is bounded (2^24 polls or 2 s): on timeout the
+// status word gets MOE_FLAG_BARRIER_TIMEOUT and the kernel returns (outputs
+// undefined; the gather that follows never stores through an out-of-range
+// position; re-initialise the workspace before its next use).
 #pragma once
 
 #include "common.cuh"
@@ -34,8 +46,11 @@ constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / kWarpSize;
 constexpr int kRouteRowsPerLane = 4;
 constexpr int kRouteRoundRows = kRouteThreads * kRouteRowsPerLane;  // 1024
-constexpr unsigned kBarrierSpinLimit = 1u << 24;                  // polls before giving up
-constexpr unsigned long long kBarrierTimeLimitNs = 2000000000ull;  // or 2 s, whichever first
+constexpr unsigned kTablePollLimit = 1u << 24;                   // polls before giving up
+constexpr unsigned long long kTableTimeLimitNs = 2000000000ull;  // or 2 s, whichever first
+constexpr int kTagShift = 24;
+constexpr unsigned kCountMask = (1u << kTagShift) - 1u;  // per-entry counts stay below 2^24
+constexpr int kPollBatch = 4;                            // table rows a thread loads at once
 
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
@@ -43,45 +58,60 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
-// Grid-wide barrier for a cooperatively launched grid.  hdr->arrive counts
-// arrivals (the last one resets it); hdr->gen is bumped once per barrier.
-// `gen` is the generation thread 0 read at kernel start: it cannot move before
-// every block of this grid has arrived.  Ordering: bar.sync gathers the
-// block's writes into thread 0, whose arrival is an acquire-release atomic;
-// the last block publishes with a release add on gen; waiters read gen with
-// acquire loads.  Returns false (and flags the status word) if the wait gave
-// up.
-__device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned gen) {
-  __shared__ int s_ok;
+__device__ __forceinline__ unsigned call_tag(unsigned gen) { return 0x80u | (gen & 0x7fu); }
+
+__device__ __forceinline__ void st_relaxed(unsigned* p, unsigned v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_relaxed_quad(const unsigned* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ bool has_tag(uint4 v, unsigned tag) {
+  return ((v.x >> kTagShift) == tag) & ((v.y >> kTagShift) == tag) &
+         ((v.z >> kTagShift) == tag) & ((v.w >> kTagShift) == tag);
+}
+
+// Re-read four table entries until all carry `tag`.  Bounded: false after
+// kTablePollLimit reads or kTableTimeLimitNs.
+__device__ __forceinline__ bool poll_quad(const unsigned* p, unsigned tag, uint4& v) {
+  unsigned long long t0 = 0;
+  for (unsigned spins = 1; spins < kTablePollLimit; ++spins) {
+    v = ld_relaxed_quad(p);
+    if (has_tag(v, tag)) return true;
+    if ((spins & 255u) == 1u) {
+      const unsigned long long now = global_ns();
+      if (spins == 1u) t0 = now;
+      else if (now - t0 > kTableTimeLimitNs) return false;
+    }
+    if (spins > 64u) __nanosleep(32);
+  }
+  return false;
+}
+
+// Block 0's last step of a call, once it has read every block's row (so every
+// block has read gen): zero the entries [ext, table_hi) an earlier call left
+// (this call reads only entries below ext), record ext, and advance gen for
+// the next call.  The release orders the gen store after the row reads; it
+// comes last because it waits for the block's earlier stores, which the
+// grid's completion waits for anyway.
+__device__ __forceinline__ void retire_table(WsHeader* hdr, unsigned* table, unsigned ext,
+                                             unsigned gen) {
+  if (blockIdx.x != 0) return;
+  unsigned hi;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(hi) : "l"(&hdr->table_hi) : "memory");
+  for (unsigned i = ext + threadIdx.x; i < hi; i += blockDim.x) st_relaxed(table + i, 0u);
   __syncthreads();
   if (threadIdx.x == 0) {
-    int ok = 1;
-    unsigned arrived;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
-                 : "=r"(arrived) : "l"(&hdr->arrive) : "memory");
-    if (arrived == gridDim.x - 1) {
-      asm volatile("st.relaxed.gpu.global.u32 [%0], 0;" :: "l"(&hdr->arrive) : "memory");
-      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" :: "l"(&hdr->gen) : "memory");
-    } else {
-      unsigned spins = 0;
-      const unsigned long long t_start = global_ns();
-      while (true) {
-        unsigned now;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(now) : "l"(&hdr->gen) : "memory");
-        if (now != gen) break;
-        if (++spins == kBarrierSpinLimit ||
-            ((spins & 1023u) == 0u && global_ns() - t_start > kBarrierTimeLimitNs)) {
-          atomicOr(&hdr->status, MOE_FLAG_BARRIER_TIMEOUT);
-          ok = 0;
-          break;
-        }
-        if (spins > 4096u) __nanosleep(64);
-      }
-    }
-    s_ok = ok;
+    st_relaxed(&hdr->table_hi, ext);
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(&hdr->gen), "r"(gen + 1u) : "memory");
   }
-  __syncthreads();
-  return s_ok != 0;
 }
 
 // Final position of a kept row whose contiguous position is p.  Contiguous
@@ -115,7 +145,7 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
              int64_t T, int K, int E, int E_local,
              int64_t* __restrict__ offsets, int32_t* __restrict__ permuted_idx,
              int32_t* __restrict__ inv_permuted_idx, WsHeader* __restrict__ hdr,
-             int* __restrict__ table, int64_t M, int32_t* __restrict__ expert_num_tokens) {
+             unsigned* __restrict__ table, int64_t M, int32_t* __restrict__ expert_num_tokens) {
   extern __shared__ int smem[];
   __shared__ int s_warp[32];
   int* s_base = smem;                 // [E_local + 1]
@@ -139,8 +169,10 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
   pdl_wait();
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
+    // Acquire: pairs with block 0's release of the next value, which comes
+    // after it has read this block's row (so this read sees the old value).
     unsigned g;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(&hdr->gen) : "memory");
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(&hdr->gen) : "memory");
     s_gen = g;
   }
   for (int e = threadIdx.x; e < E_local; e += blockDim.x) {
@@ -172,43 +204,67 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
   flags = __reduce_or_sync(kFullMask, flags);
   if (flags != 0 && lane == 0) atomicOr(&hdr->status, flags);
   __syncthreads();
-  const int e_pad = (E_local + 3) & ~3;  // table rows padded to whole int4s
+  const int e_pad = (E_local + 3) & ~3;  // table rows padded to whole 16-byte quads
+  const unsigned tag = call_tag(s_gen);
+  const unsigned tag_bits = tag << kTagShift;
   for (int e = threadIdx.x; e < e_pad; e += blockDim.x)
-    table[static_cast<int64_t>(b) * e_pad + e] = e < E_local ? s_run[e] : 0;
+    st_relaxed(table + static_cast<int64_t>(b) * e_pad + e,
+               tag_bits | (e < E_local ? static_cast<unsigned>(s_run[e]) : 0u));
 
-  // Phase 2: every block's histogram is in the table after this.
-  if (!grid_barrier(hdr, s_gen)) return;
-
-  // Phase 3: totals, offsets and this block's bases from the whole table.
+  // Phase 2: totals, offsets and this block's bases from the whole table.
   // Thread i reads 4 experts (quad i % n_quads) of the table rows
-  // bb = i / n_quads, i / n_quads + n_groups, ... with 16-byte loads.
+  // bb = i / n_quads, i / n_quads + n_groups, ..., kPollBatch rows at a time
+  // with 16-byte loads; a quad that does not carry this call's tag yet is
+  // re-read until it does.
+  bool timed_out = false;
   {
     const int n_quads = e_pad / 4;
     const int n_groups = max(1, static_cast<int>(blockDim.x) / n_quads);
-    for (int i = threadIdx.x; i < n_quads * n_groups; i += blockDim.x) {
+    for (int i = threadIdx.x; i < n_quads * n_groups && !timed_out; i += blockDim.x) {
       const int q = i % n_quads;
       const int g = i / n_quads;
-      int4 tot = make_int4(0, 0, 0, 0), bef = make_int4(0, 0, 0, 0);
-#pragma unroll 8
-      for (int bb = g; bb < B; bb += n_groups) {
-        const int4 c =
-            __ldcg(reinterpret_cast<const int4*>(table + static_cast<int64_t>(bb) * e_pad) + q);
-        tot.x += c.x; tot.y += c.y; tot.z += c.z; tot.w += c.w;
-        if (bb < b) { bef.x += c.x; bef.y += c.y; bef.z += c.z; bef.w += c.w; }
+      unsigned tot[4] = {0u, 0u, 0u, 0u}, bef[4] = {0u, 0u, 0u, 0u};
+      for (int bb0 = g; bb0 < B && !timed_out; bb0 += kPollBatch * n_groups) {
+        uint4 c[kPollBatch];
+#pragma unroll
+        for (int u = 0; u < kPollBatch; ++u) {
+          const int bb = bb0 + u * n_groups;
+          c[u] = bb < B ? ld_relaxed_quad(table + static_cast<int64_t>(bb) * e_pad + 4 * q)
+                        : make_uint4(tag_bits, tag_bits, tag_bits, tag_bits);
+        }
+#pragma unroll
+        for (int u = 0; u < kPollBatch; ++u) {
+          const int bb = bb0 + u * n_groups;
+          if (!has_tag(c[u], tag) &&
+              !poll_quad(table + static_cast<int64_t>(bb) * e_pad + 4 * q, tag, c[u])) {
+            timed_out = true;
+            break;
+          }
+          const unsigned v[4] = {c[u].x & kCountMask, c[u].y & kCountMask, c[u].z & kCountMask,
+                                 c[u].w & kCountMask};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            tot[k] += v[k];
+            if (bb < b) bef[k] += v[k];
+          }
+        }
       }
       const int e0 = q * 4;
-      const int tv[4] = {tot.x, tot.y, tot.z, tot.w};
-      const int bv[4] = {bef.x, bef.y, bef.z, bef.w};
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         if (e0 + u < E_local) {
-          atomicAdd(&s_tot[e0 + u], tv[u]);
-          atomicAdd(&s_bef[e0 + u], bv[u]);
+          atomicAdd(&s_tot[e0 + u], static_cast<int>(tot[u]));
+          atomicAdd(&s_bef[e0 + u], static_cast<int>(bef[u]));
         }
       }
     }
   }
-  __syncthreads();
+  const unsigned ext = static_cast<unsigned>(B) * static_cast<unsigned>(e_pad);
+  if (__syncthreads_or(timed_out)) {
+    if (threadIdx.x == 0) atomicOr(&hdr->status, MOE_FLAG_BARRIER_TIMEOUT);
+    retire_table(hdr, table, ext, s_gen);
+    return;
+  }
   // Exclusive scan of the totals; E_local <= MOE_MAX_LOCAL_EXPERTS, i.e. at
   // most kPer consecutive experts per thread.
   {
@@ -249,7 +305,7 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
          p < R; p += static_cast<int64_t>(B) * blockDim.x)
       permuted_idx[p] = -1;
 
-  // Phase 4: positions.
+  // Phase 3: positions.
   if (one_round) {
 #pragma unroll
     for (int j = 0; j < J; ++j) {
@@ -264,6 +320,7 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
         inv_permuted_idx[r] = p;
       }
     }
+    retire_table(hdr, table, ext, s_gen);
     return;
   }
   // More rows than one round: rank round by round; s_run[e] = this block's
@@ -303,6 +360,7 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
     }
     __syncthreads();
   }
+  retire_table(hdr, table, ext, s_gen);
 }
 
 }  // namespace moe
