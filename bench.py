@@ -73,6 +73,11 @@ def quant_permute_bytes(T, H, K, E_L, Tv, Nv, group=128):
     return T * K * 4 + Tv * H * 2 + Nv * (H + (H // group) * 4) + 2 * T * K * 4 + (E_L + 1) * 8
 
 
+def metadata_bytes(T, K, E_L):
+    """Metadata-only permute: int32 ids + both index maps + offsets."""
+    return T * K * 4 + 2 * T * K * 4 + (E_L + 1) * 8
+
+
 def unpermute_bytes(T, H, K, Nv):
     """inv + weights + kept expert rows read + output written."""
     return 2 * T * K * 4 + Nv * H * 2 + T * H * 2
@@ -260,6 +265,12 @@ class Setup:
                                       self.ws, self.qcodes, self.qscales, num_experts=self.wl.E,
                                       num_local_experts=self.wl.e_local, expert_map=self.emap)
 
+    def permute_metadata(self):
+        """Routing metadata only (no row gather): the consumer gathers rows itself."""
+        self.mp.moe_permute(None, self.ids, self.offsets, self.pidx, self.inv, self.ws,
+                            num_experts=self.wl.E, num_local_experts=self.wl.e_local,
+                            expert_map=self.emap)
+
     def permute(self):
         self.mp.moe_permute(self.hidden, self.ids, self.offsets, self.pidx, self.inv, self.ws,
                             num_experts=self.wl.E, num_local_experts=self.wl.e_local,
@@ -270,8 +281,8 @@ class Setup:
         self.mp.moe_unpermute(self.rows, self.w, self.inv, self.out, workspace=self.ws)
 
     def launches_per_permute(self):
-        """Kernels one moe_permute call launches: one up to 2048 expanded rows,
-        else the routing grid plus the gather."""
+        """Kernels one moe_permute (or moe_permute_quant_fp8) call launches: one
+        up to 2048 expanded rows, else the routing grid plus the gather."""
         return 1 if self.T * self.wl.K <= 2048 else 2
 
     def footprint(self):
@@ -343,7 +354,8 @@ def sweep(dev, peak, flush):
     sets for the smallest batches).  *_us is the device time per call from
     replaying a CUDA graph of back-to-back calls (no Python launch cost);
     *_eager_us the same calls launched one by one from Python; at T = 1 also a
-    single eager call after an L2 flush.  For the DeepSeek-V3 shape also
+    single eager call after an L2 flush.  metadata_permute_us: the routing
+    metadata alone (no row gather), a latency workload.  For the DeepSeek-V3 shape also
     quantise-on-permute from bf16 rows (quant_fp8_permute_*); for the Qwen3
     shape also the batched layout with capacity M = T (batched_permute_*)."""
     rows = []
@@ -367,6 +379,10 @@ def sweep(dev, peak, flush):
                    "unpermute_frac": round(s0.ubytes / u_us / 1e3 / peak, 4),
                    "permute_eager_us": round(back_to_back_us([s.permute for s in sets], n), 2),
                    "unpermute_eager_us": round(back_to_back_us([s.unpermute for s in sets], n), 2)}
+            m_us = graph_us([s.permute_metadata for s in sets], n_graph)
+            rec["metadata_permute_us"] = round(m_us, 2)
+            rec["metadata_permute_GBps"] = round(
+                metadata_bytes(T, s0.wl.K, s0.wl.e_local) / m_us / 1e3, 1)
             if name == "qwen3" and T >= 1024:
                 for st in sets:
                     st.enable_batched(dev, T)
@@ -512,7 +528,7 @@ def main():
             st.enable_quant(dev)
     perm_bytes = s0.qbytes if args.quant else s0.pbytes
     step_bytes = perm_bytes + s0.ubytes
-    launches_per_step = (2 if args.quant else s0.launches_per_permute()) + 1
+    launches_per_step = s0.launches_per_permute() + 1
 
     def do_permute(s):
         if args.quant:

@@ -10,7 +10,7 @@ import ctypes
 import os
 import threading
 
-from .build import LIB_PATH
+from .build import DEBUG_LIB_PATH, LIB_PATH
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = -1
@@ -66,7 +66,15 @@ SIGNATURES = {
 
 MOE_NOALLOC_SCRATCH_BYTES = (1 << 20) + 256
 
+# Exported by the debug build only (include/moe_permute_debug.h).
+DEBUG_SIGNATURES = {
+    "moe_debug_set_table_wait": (ctypes.c_int, [ctypes.c_int, ctypes.c_ulonglong]),
+}
+MOE_DEBUG_MAX_EXTRA_ROWS = 4
+TABLE_WAIT_NS = 2_000_000_000  # the production limit of a routing-table wait
+
 _lib = None
+_debug_lib = None
 _lock = threading.Lock()
 
 
@@ -100,6 +108,24 @@ def lib() -> ctypes.CDLL:
                     fn.argtypes = args
                 _lib = handle
     return _lib
+
+
+def debug_lib() -> ctypes.CDLL:
+    """The debug build (same entry points plus the test hook); for tests."""
+    global _debug_lib
+    if _debug_lib is None:
+        with _lock:
+            if _debug_lib is None:
+                if not os.path.exists(DEBUG_LIB_PATH):
+                    raise RuntimeError(f"{DEBUG_LIB_PATH} is missing: build it with "
+                                       "`python -c 'import __graft_entry__ as g; g.build()'`")
+                handle = ctypes.CDLL(DEBUG_LIB_PATH)
+                for name, (res, args) in {**SIGNATURES, **DEBUG_SIGNATURES}.items():
+                    fn = getattr(handle, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _debug_lib = handle
+    return _debug_lib
 
 
 def status_string(status: int) -> str:

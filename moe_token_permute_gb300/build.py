@@ -1,8 +1,10 @@
-"""Build libmoe_permute.so (the C-ABI CUDA library) in-tree with nvcc.
+"""Build libmoe_permute.so (the C-ABI CUDA library) in-tree with nvcc, and
+beside it libmoe_permute_debug.so, the same sources with -DMOE_DEBUG_HOOKS
+(the test hook of include/moe_permute_debug.h).  The two compile in parallel.
 
 Usage: python -m moe_token_permute_gb300.build [--verbose]
-Target: sm_103a only (GB300).  The library is linked against the shared CUDA
-runtime so it shares one runtime with the host process.
+Target: sm_103a only (GB300).  The libraries are linked against the shared
+CUDA runtime so they share one runtime with the host process.
 """
 from __future__ import annotations
 
@@ -19,6 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libmoe_permute.so"
 LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
+DEBUG_LIB_PATH = os.path.join(OUT_DIR, "libmoe_permute_debug.so")
 SOURCES = ["moe_permute_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -42,33 +45,49 @@ def _cuda_lib_dir(nvcc: str) -> str:
 def _inputs():
     files = [os.path.join(CSRC, s) for s in SOURCES]
     files += glob.glob(os.path.join(CSRC, "*.cuh"))
-    files += [os.path.join(INCLUDE, "moe_permute.h"), os.path.abspath(__file__)]
+    files += glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
+def _command(nvcc: str, out: str, defines, verbose: bool):
+    cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared",
+           "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden", *defines,
+           "-I", INCLUDE, "-I", CSRC, "-cudart", "shared",
+           "-Xlinker", "-rpath," + _cuda_lib_dir(nvcc),
+           "-o", out] + [os.path.join(CSRC, s) for s in SOURCES]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+    return cmd
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the library if it is missing or older than its sources."""
-    if not force and up_to_date():
+    """Compile the libraries that are missing or older than their sources
+    (both nvcc runs in parallel); returns the production library's path."""
+    targets = [(LIB_PATH, []), (DEBUG_LIB_PATH, ["-DMOE_DEBUG_HOOKS"])]
+    todo = [(path, d) for path, d in targets if force or not up_to_date(path)]
+    if not todo:
         return LIB_PATH
     nvcc = _nvcc()
     os.makedirs(OUT_DIR, exist_ok=True)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-shared",
-           "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
-           "-I", INCLUDE, "-I", CSRC, "-cudart", "shared",
-           "-Xlinker", "-rpath," + _cuda_lib_dir(nvcc),
-           "-o", tmp] + [os.path.join(CSRC, s) for s in SOURCES]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    subprocess.check_call(cmd)
-    os.replace(tmp, LIB_PATH)
+    jobs = []
+    for path, defines in todo:
+        tmp = path + f".tmp{os.getpid()}"
+        jobs.append((subprocess.Popen(_command(nvcc, tmp, defines, verbose)), tmp, path))
+    failed = []
+    for proc, tmp, path in jobs:
+        if proc.wait() != 0:
+            failed.append(path)
+        else:
+            os.replace(tmp, path)
+    if failed:
+        raise RuntimeError(f"nvcc failed building {', '.join(failed)}")
     return LIB_PATH
 
 

@@ -10,9 +10,13 @@
 //   R = T*K <= kFusedMaxRows: one launch of k_permute_fused; every block
 //     redundantly ranks all rows and the blocks share the row copy (no
 //     inter-block communication);
-//   otherwise: k_route_coop (cooperative grid, one grid barrier) writes the
-//     metadata, and k_gather_rows, launched as its programmatic dependent,
-//     loads rows while the routing runs and stores them once it has finished.
+//   otherwise: k_route_coop (cooperative grid; its blocks exchange their
+//     histograms through a tagged table in the workspace) writes the
+//     metadata, and the row gather (k_gather_rows_tma or k_gather_rows),
+//     launched as its programmatic dependent, loads rows while the routing
+//     runs and stores them once it has finished.
+//   moe_permute_quant_fp8 splits the same way: k_permute_fused with its
+//   quantising copy, or k_route_coop + k_gather_quant_fp8.
 // Every launch carries programmatic stream serialization, so its launch
 // latency overlaps the previous kernel's tail.
 #include <cuda_runtime.h>
@@ -23,6 +27,9 @@
 #include <mutex>
 
 #include "moe_permute.h"
+#ifdef MOE_DEBUG_HOOKS
+#include "moe_permute_debug.h"
+#endif
 #include "common.cuh"
 #include "routing.cuh"
 #include "rows.cuh"
@@ -111,6 +118,10 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 constexpr int64_t kCoopMaxBlocks = 1024;  // table rows reserved for the cooperative grid
 
+#ifdef MOE_DEBUG_HOOKS
+int g_debug_extra_rows_host = 0;  // host copy of the routing grid's g_debug_extra_rows
+#endif
+
 // Header plus the cooperative kernel's per-block histogram table
 // [min(max_tokens, kCoopMaxBlocks)][num_experts rounded up to 4].
 size_t workspace_bytes_for(int64_t max_tokens, int32_t topk, int32_t num_experts) {
@@ -154,7 +165,7 @@ unsigned item_grid(int64_t items, int warps_per_block, const DeviceInfo* d, int 
   return static_cast<unsigned>(std::max<int64_t>(1, std::min(need, cap)));
 }
 
-template <typename IdT, typename VecT, int V>
+template <typename IdT, typename VecT, int V, bool kQuant = false>
 cudaError_t launch_fused(const IdT* ids, const int32_t* emap, int64_t T, int K, int E, int E_local,
                          const void* hidden, int64_t row_bytes, const float* scales,
                          int64_t scale_cols, void* out, float* out_scales, int64_t* offsets,
@@ -163,7 +174,7 @@ cudaError_t launch_fused(const IdT* ids, const int32_t* emap, int64_t T, int K, 
   const int64_t R = T * K;
   const int64_t rank_warps = ceil_div(R, 32 * kMetaRowsPerLane);
   const size_t smem = (static_cast<size_t>(rank_warps) * E_local + E_local + 1 + R) * sizeof(int);
-  auto kern = k_permute_fused<IdT, VecT, V>;
+  auto kern = k_permute_fused<IdT, VecT, V, kQuant>;
   cudaError_t err = allow_smem(kern, smem);
   if (err != cudaSuccess) return err;
   const int64_t row_vecs = row_bytes / static_cast<int64_t>(sizeof(VecT));
@@ -194,6 +205,11 @@ cudaError_t launch_route(const IdT* ids, const int32_t* emap, int64_t T, int K, 
   B = std::max(B, ceil_div(T, static_cast<int64_t>(kCountMask) / K));
   B = std::max<int64_t>(1, std::min(B, kCoopMaxBlocks));
   if (ceil_div(T, B) * K > static_cast<int64_t>(kCountMask)) return cudaErrorInvalidConfiguration;
+#ifdef MOE_DEBUG_HOOKS
+  // The extra rows the blocks wait for must lie inside the workspace's table,
+  // which holds min(T, kCoopMaxBlocks) rows.
+  if (B + g_debug_extra_rows_host > std::min(T, kCoopMaxBlocks)) return cudaErrorInvalidValue;
+#endif
   unsigned* table = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(hdr) + kWsHeaderBytes);
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
@@ -258,17 +274,37 @@ cudaError_t launch_gather_tma(const void* hidden, int64_t row_bytes, const float
                 inv, T, K, static_cast<char*>(out), out_scales, num_out_rows, status);
 }
 
+// Expected rows written per source row: K, scaled by the kept share of the
+// experts when an expert map drops some.
+double writes_per_row(int K, int E, int E_local, const int32_t* emap) {
+  return emap == nullptr ? static_cast<double>(K)
+                         : static_cast<double>(K) * static_cast<double>(E_local) / E;
+}
+
+// Source bytes, as a multiple of the bulk-copy gather's prefetch, up to which
+// it beats the register gather.  The bulk-copy gather loads most rows while
+// routing runs, but its stores of each chunk come from one warp; the register
+// gather keeps more stores in flight.  So the crossover falls as the rows
+// written per source row grow (measured on GB300: about 2x at 1-2 writes per
+// row, 1.1-1.25x at 8, the lower end for 4 KB rows, which the register
+// gather moves in whole chunks).  writes_per_row: K, or K * E_local / E with
+// an expert map (uniform routing).
+double tma_max_ratio(double writes_per_row) {
+  return std::min(2.0, std::max(1.15, 2.0 - (writes_per_row - 2.0) * 0.85 / 6.0));
+}
+
 // The row gather for any vector width: out rows are indexed by inv values in
 // [0, num_out_rows).  16-byte aligned rows go through the bulk-copy engine
-// when most of the source rows fit its prefetch (it then loads them while the
-// routing grid runs); larger batches keep more loads in flight with the
-// register gather.
+// when the source rows fit its prefetch well enough (tma_max_ratio); larger
+// batches keep more loads in flight with the register gather.
 cudaError_t launch_gather_any(size_t vb, const void* hidden, int64_t row_bytes,
                               const float* scales, int64_t scale_cols, const int32_t* inv,
-                              int64_t T, int K, void* out, float* out_scales,
-                              int64_t num_out_rows, unsigned* status, const DeviceInfo* d,
-                              cudaStream_t s) {
-  if (vb == 16 && 2 * T * row_bytes <= 3 * tma_geometry(row_bytes, T, d).prefetch_bytes)
+                              int64_t T, int K, double writes_per_row, void* out,
+                              float* out_scales, int64_t num_out_rows, unsigned* status,
+                              const DeviceInfo* d, cudaStream_t s) {
+  if (vb == 16 && static_cast<double>(T * row_bytes) <=
+                      tma_max_ratio(writes_per_row) *
+                          static_cast<double>(tma_geometry(row_bytes, T, d).prefetch_bytes))
     return launch_gather_tma(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales,
                              num_out_rows, status, d, s);
   switch (vb) {
@@ -300,8 +336,9 @@ cudaError_t permute_typed(const IdT* ids, const int32_t* emap, int64_t T, int K,
   }
   cudaError_t err = launch_route<IdT>(ids, emap, T, K, E, E_local, offsets, pidx, inv, hdr, d, s);
   if (err != cudaSuccess || out == nullptr) return err;
-  return launch_gather_any(vb, hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales,
-                           R, &hdr->status, d, s);
+  return launch_gather_any(vb, hidden, row_bytes, scales, scale_cols, inv, T, K,
+                           writes_per_row(K, E, E_local, emap), out, out_scales, R, &hdr->status,
+                           d, s);
 }
 
 template <typename IdT>
@@ -314,7 +351,8 @@ cudaError_t permute_batched_typed(const IdT* ids, const int32_t* emap, int64_t T
                                       static_cast<WsHeader*>(ws), d, s, M, counts);
   if (err != cudaSuccess || out == nullptr) return err;
   const size_t vb = vec_bytes(row_bytes, hidden, out);
-  return launch_gather_any(vb, hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales,
+  return launch_gather_any(vb, hidden, row_bytes, scales, scale_cols, inv, T, K,
+                           writes_per_row(K, E, E_local, emap), out, out_scales,
                            static_cast<int64_t>(E_local) * M,
                            &static_cast<WsHeader*>(ws)->status, d, s);
 }
@@ -326,6 +364,10 @@ cudaError_t permute_quant_typed(const IdT* ids, const int32_t* emap, int64_t T, 
                                 int E_local, const void* hidden, int64_t H, void* codes,
                                 float* scales, int64_t* offsets, int32_t* pidx, int32_t* inv,
                                 void* ws, const DeviceInfo* d, cudaStream_t s) {
+  if (T * K <= kFusedMaxRows)
+    return launch_fused<IdT, uint4, kFusedV, true>(ids, emap, T, K, E, E_local, hidden, H * 2,
+                                                   nullptr, 0, codes, scales, offsets, pidx, inv,
+                                                   static_cast<WsHeader*>(ws), d, s);
   cudaError_t err = launch_route<IdT>(ids, emap, T, K, E, E_local, offsets, pidx, inv,
                                       static_cast<WsHeader*>(ws), d, s);
   if (err != cudaSuccess) return err;
@@ -697,3 +739,18 @@ extern "C" int moe_permute_noalloc(const void* hidden_states, moe_dtype_t hidden
                      expert_first_token_offset, permuted_idx, inv_permuted_idx, scratch,
                      MOE_NOALLOC_SCRATCH_BYTES, stream);
 }
+
+#ifdef MOE_DEBUG_HOOKS
+extern "C" int moe_debug_set_table_wait(int extra_rows, unsigned long long wait_ns) {
+  if (extra_rows < 0 || extra_rows > MOE_DEBUG_MAX_EXTRA_ROWS || wait_ns == 0)
+    return MOE_ERR_INVALID_ARG;
+  if (cudaMemcpyToSymbol(moe::g_debug_extra_rows, &extra_rows, sizeof(extra_rows)) !=
+          cudaSuccess ||
+      cudaMemcpyToSymbol(moe::g_debug_table_wait_ns, &wait_ns, sizeof(wait_ns)) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  moe::g_debug_extra_rows_host = extra_rows;
+  return MOE_OK;
+}
+#endif

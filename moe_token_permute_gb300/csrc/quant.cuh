@@ -25,35 +25,19 @@ namespace moe {
 constexpr int kQuantGroup = 128;  // columns per scale
 constexpr float kE4m3Max = 448.0f;
 
+// Quantise one (token, chunk) item held in registers (V vectors of 8 bf16
+// values per lane; lanes 0-15 and 16-31 of vector slot i cover one 128-column
+// group each) and store codes and scales to every destination row p_k whose
+// bit k is set in `valid` (lane k < K holds p_k in `p`).  Every lane of the
+// warp must call it (the group maxima are half-warp shuffles); vectors at or
+// beyond row_vecs are not stored.
 template <int V>
-__global__ void __launch_bounds__(256)
-k_gather_quant_fp8(const uint4* __restrict__ hidden, int64_t row_vecs,
-                   const int32_t* __restrict__ inv_permuted_idx, int64_t T, int K,
-                   uint2* __restrict__ out_codes, float* __restrict__ out_scales,
-                   int64_t num_out_rows) {
-  constexpr int64_t kChunk = 32 * V;  // vectors of 8 values per item
+__device__ __forceinline__ void quant_store_chunk(const uint4 (&v)[V], int64_t c0,
+                                                  int64_t row_vecs, int p, unsigned valid,
+                                                  uint2* __restrict__ out_codes,
+                                                  float* __restrict__ out_scales) {
   const int lane = threadIdx.x & 31;
-  const int64_t n_chunks = (row_vecs + kChunk - 1) / kChunk;
-  const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (item >= T * n_chunks) return;
-  const int64_t t = item / n_chunks;
-  const int64_t c0 = (item - t * n_chunks) * kChunk;
   const int64_t n_groups = row_vecs / (kQuantGroup / 8);
-
-  uint4 v[V];
-#pragma unroll
-  for (int i = 0; i < V; ++i) {
-    const int64_t c = c0 + i * 32 + lane;
-    v[i] = c < row_vecs ? ld_stream(hidden + t * row_vecs + c) : make_uint4(0, 0, 0, 0);
-  }
-  // The rows are the caller's input (complete: the routing grid has passed its
-  // own dependency wait); the positions come from the routing grid.
-  pdl_wait();
-  int p = lane < K ? __ldcg(inv_permuted_idx + t * K + lane) : -1;
-  if (p >= num_out_rows) p = -1;  // only a routing grid that gave up leaves such values
-  const unsigned valid = __ballot_sync(kFullMask, p >= 0);
-  if (valid == 0u) return;
-
 #pragma unroll
   for (int i = 0; i < V; ++i) {
     const int64_t c = c0 + i * 32 + lane;
@@ -90,6 +74,37 @@ k_gather_quant_fp8(const uint4* __restrict__ hidden, int64_t row_vecs,
       }
     }
   }
+}
+
+template <int V>
+__global__ void __launch_bounds__(256)
+k_gather_quant_fp8(const uint4* __restrict__ hidden, int64_t row_vecs,
+                   const int32_t* __restrict__ inv_permuted_idx, int64_t T, int K,
+                   uint2* __restrict__ out_codes, float* __restrict__ out_scales,
+                   int64_t num_out_rows) {
+  constexpr int64_t kChunk = 32 * V;  // vectors of 8 values per item
+  const int lane = threadIdx.x & 31;
+  const int64_t n_chunks = (row_vecs + kChunk - 1) / kChunk;
+  const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (item >= T * n_chunks) return;
+  const int64_t t = item / n_chunks;
+  const int64_t c0 = (item - t * n_chunks) * kChunk;
+
+  uint4 v[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int64_t c = c0 + i * 32 + lane;
+    v[i] = c < row_vecs ? ld_stream(hidden + t * row_vecs + c) : make_uint4(0, 0, 0, 0);
+  }
+  // The rows are the caller's input (complete: the routing grid has passed its
+  // own dependency wait); the positions come from the routing grid.
+  pdl_wait();
+  int p = lane < K ? __ldcg(inv_permuted_idx + t * K + lane) : -1;
+  if (p >= num_out_rows) p = -1;  // only a routing grid that gave up leaves such values
+  const unsigned valid = __ballot_sync(kFullMask, p >= 0);
+  if (valid == 0u) return;
+
+  quant_store_chunk<V>(v, c0, row_vecs, p, valid, out_codes, out_scales);
 }
 
 }  // namespace moe

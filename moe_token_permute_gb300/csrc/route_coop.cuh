@@ -58,6 +58,21 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
+#ifdef MOE_DEBUG_HOOKS
+// Debug builds only (moe_debug_set_table_wait): table rows past the grid
+// that every block also waits for -- rows no block writes, so the waits run
+// out -- and the time limit of a wait.
+__device__ int g_debug_extra_rows = 0;
+__device__ unsigned long long g_debug_table_wait_ns = kTableTimeLimitNs;
+__device__ __forceinline__ int debug_extra_rows() { return g_debug_extra_rows; }
+__device__ __forceinline__ unsigned long long table_time_limit_ns() {
+  return g_debug_table_wait_ns;
+}
+#else
+__device__ __forceinline__ int debug_extra_rows() { return 0; }
+__device__ __forceinline__ unsigned long long table_time_limit_ns() { return kTableTimeLimitNs; }
+#endif
+
 __device__ __forceinline__ unsigned call_tag(unsigned gen) { return 0x80u | (gen & 0x7fu); }
 
 __device__ __forceinline__ void st_relaxed(unsigned* p, unsigned v) {
@@ -88,7 +103,7 @@ __device__ __forceinline__ bool poll_quad(const unsigned* p, unsigned tag, uint4
     if ((spins & 255u) == 1u) {
       const unsigned long long now = global_ns();
       if (spins == 1u) t0 = now;
-      else if (now - t0 > kTableTimeLimitNs) return false;
+      else if (now - t0 > table_time_limit_ns()) return false;
     }
     if (spins > 64u) __nanosleep(32);
   }
@@ -218,18 +233,19 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
   // re-read until it does.
   bool timed_out = false;
   {
+    const int B_read = B + debug_extra_rows();  // B outside debug builds
     const int n_quads = e_pad / 4;
     const int n_groups = max(1, static_cast<int>(blockDim.x) / n_quads);
     for (int i = threadIdx.x; i < n_quads * n_groups && !timed_out; i += blockDim.x) {
       const int q = i % n_quads;
       const int g = i / n_quads;
       unsigned tot[4] = {0u, 0u, 0u, 0u}, bef[4] = {0u, 0u, 0u, 0u};
-      for (int bb0 = g; bb0 < B && !timed_out; bb0 += kPollBatch * n_groups) {
+      for (int bb0 = g; bb0 < B_read && !timed_out; bb0 += kPollBatch * n_groups) {
         uint4 c[kPollBatch];
 #pragma unroll
         for (int u = 0; u < kPollBatch; ++u) {
           const int bb = bb0 + u * n_groups;
-          c[u] = bb < B ? ld_relaxed_quad(table + static_cast<int64_t>(bb) * e_pad + 4 * q)
+          c[u] = bb < B_read ? ld_relaxed_quad(table + static_cast<int64_t>(bb) * e_pad + 4 * q)
                         : make_uint4(tag_bits, tag_bits, tag_bits, tag_bits);
         }
 #pragma unroll

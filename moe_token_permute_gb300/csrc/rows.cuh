@@ -16,6 +16,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "quant.cuh"
 #include "routing.cuh"
 
 namespace moe {
@@ -112,7 +113,11 @@ k_gather_rows(const VecT* __restrict__ hidden, int64_t row_vecs,
 // ids come from L2), block 0 writes the metadata, and all blocks share the
 // row copy: no block ever waits for another.
 // Shared memory: cnt [n_rank_warps][E_local] | s_base [E_local + 1] | s_p [R].
-template <typename IdT, typename VecT, int V>
+// kQuant: quantise-on-permute (VecT = uint4 of 8 bf16 values): each row is
+// written as fp8 e4m3 codes (permuted_hidden reinterpreted as uint2) plus one
+// fp32 scale per 128 columns (permuted_scales), by the same arithmetic as
+// k_gather_quant_fp8.
+template <typename IdT, typename VecT, int V, bool kQuant = false>
 __global__ void __launch_bounds__(kMetaThreads, 1)
 k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
                 int64_t T, int K, int E, int E_local,
@@ -196,10 +201,20 @@ k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
     const unsigned valid = __ballot_sync(kFullMask, p >= 0);
     if (valid == 0u) continue;
     VecT v[V];
-    load_chunk<VecT, V>(hidden + t * row_vecs, c0, row_vecs, v);
-    store_chunk<VecT, V>(v, permuted_hidden, c0, row_vecs, p, valid);
-    if (permuted_scales != nullptr && c0 == 0)
-      copy_token_scales(scales + t * scale_cols, scale_cols, permuted_scales, p, valid);
+    if constexpr (kQuant) {
+#pragma unroll
+      for (int i = 0; i < V; ++i) {
+        const int64_t c = c0 + i * 32 + lane;
+        v[i] = c < row_vecs ? ld_stream(hidden + t * row_vecs + c) : make_uint4(0, 0, 0, 0);
+      }
+      quant_store_chunk<V>(v, c0, row_vecs, p, valid, reinterpret_cast<uint2*>(permuted_hidden),
+                           permuted_scales);
+    } else {
+      load_chunk<VecT, V>(hidden + t * row_vecs, c0, row_vecs, v);
+      store_chunk<VecT, V>(v, permuted_hidden, c0, row_vecs, p, valid);
+      if (permuted_scales != nullptr && c0 == 0)
+        copy_token_scales(scales + t * scale_cols, scale_cols, permuted_scales, p, valid);
+    }
   }
 }
 

@@ -20,9 +20,14 @@ def lib():
     return b.lib()
 
 
-def declared_symbols():
+DEBUG_HEADER = "moe_permute_debug.h"  # exported by the debug build only
+
+
+def declared_symbols(debug=False):
     names = set()
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        if (os.path.basename(h) == DEBUG_HEADER) != debug:
+            continue
         with open(h) as f:
             text = f.read()
         names |= set(re.findall(r"MOE_API\s+[\w\s\*]*?\b(moe_\w+)\s*\(", text))
@@ -42,6 +47,22 @@ def test_every_declared_symbol_is_exported(lib):
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/ but not exported"
         assert n in b.SIGNATURES, f"{n} has no ctypes signature in the binding"
+
+
+def test_debug_hook_only_in_debug_build(lib):
+    debug_names = declared_symbols(debug=True)
+    assert debug_names == {"moe_debug_set_table_wait"}
+    for n in debug_names:
+        assert not hasattr(lib, n), f"{n} leaked into the production library"
+    dlib = b.debug_lib()
+    for n in declared_symbols() | debug_names:
+        assert hasattr(dlib, n), f"{n} missing from the debug library"
+        assert n in b.SIGNATURES or n in b.DEBUG_SIGNATURES
+
+
+@pytest.mark.parametrize("args", [(-1, 1000), (b.MOE_DEBUG_MAX_EXTRA_ROWS + 1, 1000), (1, 0)])
+def test_debug_hook_rejects_bad_arguments_on_host(lib, args):
+    assert b.debug_lib().moe_debug_set_table_wait(*args) == b.MOE_ERR_INVALID_ARG
 
 
 def test_library_built_for_sm103a_only():

@@ -54,8 +54,10 @@ def oracle_quant_permute(hidden, inp):
                           E_local=wl.e_local, hidden=q, scales=s)
 
 
-CASES = [("dsv3", 1), ("dsv3", 128), ("dsv3", 4096), ("qwen3", 1024), ("mixtral", 512),
-         ("dsv2lite", 256), ("dsv2lite", 8192), ("tiny", 16)]
+# T*K <= 2048 takes the single-launch kernel, above it the routing grid plus
+# the quantising gather: dsv3 T=256 / 257 (K=8) straddle the boundary.
+CASES = [("dsv3", 1), ("dsv3", 128), ("dsv3", 256), ("dsv3", 257), ("dsv3", 4096),
+         ("qwen3", 1024), ("mixtral", 512), ("dsv2lite", 256), ("dsv2lite", 8192), ("tiny", 16)]
 
 
 @pytest.mark.parametrize("name,T", CASES, ids=[f"{n}-T{T}" for n, T in CASES])
@@ -71,9 +73,10 @@ def test_quant_permute_matches_oracle(name, T):
     assert mp.moe_read_status(bufs["ws"]) == 0
 
 
-def test_quant_permute_int64_ids_and_one_group_rows():
-    inp = make_inputs("qwen3", 300, seed=6, with_rows=False)
-    hidden = bf16_rows(300, G, seed=3)  # H = 128: a single group per row
+@pytest.mark.parametrize("T", [200, 300])  # single launch, routing grid + gather
+def test_quant_permute_int64_ids_and_one_group_rows(T):
+    inp = make_inputs("qwen3", T, seed=6, with_rows=False)
+    hidden = bf16_rows(T, G, seed=3)  # H = 128: a single group per row
     ref = oracle_quant_permute(hidden, inp)
     bufs, codes, scales = run_quant(hidden, inp, ids_dtype=torch.int64)
     assert_metadata_equal(bufs, ref)
