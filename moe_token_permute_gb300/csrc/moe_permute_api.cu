@@ -24,7 +24,9 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "moe_permute.h"
 #ifdef MOE_DEBUG_HOOKS
@@ -141,20 +143,29 @@ int64_t row_items(int64_t T, int64_t row_vecs, int V) {
   return T * std::max<int64_t>(1, ceil_div(row_vecs, 32 * static_cast<int64_t>(V)));
 }
 
-// Resident blocks per SM of a kernel (queried once per device and kernel).
-template <typename Kern>
-int blocks_per_sm(Kern kern, int threads, size_t smem) {
-  static int cache[kMaxDevices] = {0};
+// Resident blocks per SM of a kernel, queried once per (device, kernel,
+// block size, shared memory).  The key is the kernel's address: template
+// instantiations with the same signature are different kernels.
+int blocks_per_sm(const void* kern, int threads, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, int, size_t>, int> cache;
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= kMaxDevices) return 1;
-  if (cache[dev] == 0) {
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess || n < 1)
-      n = 1;
-    cache[dev] = n;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
   }
-  return cache[dev];
+  const auto key = std::make_tuple(dev, kern, threads, smem);
+  std::lock_guard<std::mutex> lock(mu);
+  const auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess ||
+      n < 1) {
+    cudaGetLastError();
+    n = 1;
+  }
+  cache[key] = n;
+  return n;
 }
 
 // Grid for a warp-per-item kernel: one warp per item, capped at one wave of
@@ -385,8 +396,16 @@ cudaError_t launch_unpermute_kv(const void* rows, int64_t num_rows, int64_t H, c
                                 unsigned* status, const DeviceInfo* d, cudaStream_t s) {
   const int64_t row_vecs = H * 2 / static_cast<int64_t>(sizeof(VecT));
   auto kern = k_unpermute<VecT, KG, V>;
-  const unsigned grid = item_grid(row_items(T, row_vecs, V), kRowWarps, d,
-                                  blocks_per_sm(kern, kRowThreads, 0));
+  const int64_t items = row_items(T, row_vecs, V);
+  int per_sm = blocks_per_sm(reinterpret_cast<const void*>(kern), kRowThreads, 0);
+  // A fourth block per SM adds loads in flight, which pays when a warp's
+  // kept rows do not fill its KG * V vectors (K < 8: fewer rows per token,
+  // or rows dropped by an expert map) or when there are few items per warp.
+  // With K >= 8 dense rows and many items per warp it measured 1-3% slower
+  // on GB300 (more streams competing for DRAM), so those keep three.
+  if (per_sm > 3 && K >= 8 && items > 6 * static_cast<int64_t>(d->sm_count) * 3 * kRowWarps)
+    per_sm = 3;
+  const unsigned grid = item_grid(items, kRowWarps, d, per_sm);
   return launch(kern, grid, kRowThreads, 0, s, static_cast<const VecT*>(rows), num_rows, row_vecs,
                 w, inv, T, K, static_cast<VecT*>(out), status);
 }

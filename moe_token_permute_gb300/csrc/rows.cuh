@@ -231,9 +231,12 @@ struct Bf16Vec {
 // Unpermute: warp per (token, chunk).  k ascending, fp32 multiply then fp32
 // add per term (no contraction), one bf16 round-to-nearest-even at the end.
 // The loads of up to KG kept rows are in flight together; KG * V is kept near
-// 8 vectors per lane whatever K is.
+// 8 vectors per lane whatever K is.  With V <= 2 the kernel fits 64 registers
+// without spilling, so 4 blocks of 256 threads can share an SM (the launch
+// decides whether to use the fourth).  V = 4 keeps 3 blocks (80 registers;
+// without a bound the compiler spends 122 and only 2 fit), V = 8 needs 2.
 template <typename VecT, int KG, int V>
-__global__ void __launch_bounds__(kRowThreads)
+__global__ void __launch_bounds__(kRowThreads, V <= 2 ? 4 : (V <= 4 ? 3 : 2))
 k_unpermute(const VecT* __restrict__ rows, int64_t num_rows, int64_t row_vecs,
             const float* __restrict__ topk_weights, const int32_t* __restrict__ inv_permuted_idx,
             int64_t T, int K, VecT* __restrict__ out, unsigned* __restrict__ status) {
