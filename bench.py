@@ -291,6 +291,97 @@ class Setup:
         return sum(t.numel() * t.element_size() for t in ts if t is not None)
 
 
+class EndToEnd:
+    """A step from pinned host memory to pinned host memory through the public
+    API: every step copies its inputs in (hidden rows, ids, weights, the expert
+    rows unpermute reads), runs moe_permute + moe_unpermute, and copies the
+    output and the expert offsets out.
+
+    serial_ms: everything on one stream, one step after another.
+    pipelined_ms: a serving-style schedule over two device buffer sets.  Step
+    i's inputs go in on a copy stream while step i-1 computes, its kernels run
+    on a compute stream, and its results come out on a second copy stream; a
+    set is refilled only once its previous step's kernels and copies out are
+    done.  Same bytes, same calls."""
+
+    def __init__(self, sets, do_permute, quant):
+        self.sets, self.do_permute = sets, do_permute
+        self.dev_in = [[st.qhidden if quant else st.hidden, st.ids, st.w, st.rows] for st in sets]
+        s0 = sets[0]
+        self.h_in = [t.cpu().pin_memory() for t in self.dev_in[0]]
+        self.h_out = [torch.empty_like(s0.out, device="cpu").pin_memory(),
+                      torch.empty_like(s0.offsets, device="cpu").pin_memory()]
+        self.h2d = sum(t.numel() * t.element_size() for t in self.h_in)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.h_out)
+
+    def _copy_in(self, j):
+        for d, h in zip(self.dev_in[j], self.h_in):
+            d.copy_(h, non_blocking=True)
+
+    def _compute(self, j):
+        st = self.sets[j]
+        self.do_permute(st)
+        st.unpermute()
+
+    def _copy_out(self, j):
+        st = self.sets[j]
+        self.h_out[0].copy_(st.out, non_blocking=True)
+        self.h_out[1].copy_(st.offsets, non_blocking=True)
+
+    @staticmethod
+    def _timed(fn, n):
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn(n)
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    def serial_ms(self, n):
+        def run(k):
+            for _ in range(k):
+                self._copy_in(0)
+                self._compute(0)
+                self._copy_out(0)
+        run(3)
+        return self._timed(run, n)
+
+    def pipelined_ms(self, n):
+        cur = torch.cuda.current_stream()
+        s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        n_sets = len(self.sets)
+
+        def run(k):
+            start = torch.cuda.Event()
+            start.record(cur)
+            for st in (s_in, s_cmp, s_out):
+                st.wait_event(start)
+            in_done = [torch.cuda.Event() for _ in range(n_sets)]
+            out_done = [None] * n_sets
+            for i in range(k):
+                j = i % n_sets
+                if out_done[j] is not None:
+                    s_in.wait_event(out_done[j])  # set j's previous step is fully done
+                with torch.cuda.stream(s_in):
+                    self._copy_in(j)
+                in_done[j].record(s_in)
+                s_cmp.wait_event(in_done[j])
+                with torch.cuda.stream(s_cmp):
+                    self._compute(j)
+                cmp_done = torch.cuda.Event()
+                cmp_done.record(s_cmp)
+                s_out.wait_event(cmp_done)
+                with torch.cuda.stream(s_out):
+                    self._copy_out(j)
+                out_done[j] = torch.cuda.Event()
+                out_done[j].record(s_out)
+            for st in (s_in, s_cmp, s_out):
+                cur.wait_stream(st)
+        run(3)
+        return self._timed(run, n)
+
+
 L2_BYTES = 129 * 1024 * 1024
 
 
@@ -581,38 +672,12 @@ def main():
     unp_us = 1e3 * sum(e[1].elapsed_time(e[2]) for e in ev) / n
 
     # end to end: pinned host inputs in, result out, every step
-    d_hidden = s0.qhidden if args.quant else s0.hidden
-    h_hidden = d_hidden.cpu().pin_memory()
-    h_ids = s0.ids.cpu().pin_memory()
-    h_w = s0.w.cpu().pin_memory()
-    h_rows = s0.rows.cpu().pin_memory()
-    h_out = torch.empty_like(s0.out, device="cpu").pin_memory()
-    h_off = torch.empty_like(s0.offsets, device="cpu").pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_hidden, h_ids, h_w, h_rows))
-    d2h = h_out.numel() * h_out.element_size() + h_off.numel() * h_off.element_size()
-
-    def e2e_step():
-        d_hidden.copy_(h_hidden, non_blocking=True)
-        s0.ids.copy_(h_ids, non_blocking=True)
-        s0.w.copy_(h_w, non_blocking=True)
-        s0.rows.copy_(h_rows, non_blocking=True)
-        do_permute(s0)
-        s0.unpermute()
-        h_out.copy_(s0.out, non_blocking=True)
-        h_off.copy_(s0.offsets, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
     n_e2e = min(n, 50)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(n_e2e):
-        e2e_step()
-    b.record()
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(a.elapsed_time(b) / n_e2e, dist, dev)
+    e2e = EndToEnd(sets, do_permute, args.quant)
+    e2e_serial_ms = max_over_ranks(e2e.serial_ms(n_e2e), dist, dev)
+    e2e_ms = max_over_ranks(e2e.pipelined_ms(n_e2e), dist, dev)
     e2e_value = job_gbs(world, step_bytes, e2e_ms)
+    h2d, d2h = e2e.h2d, e2e.d2h
 
     line = None
     if rank == 0:
@@ -645,12 +710,17 @@ def main():
                          "peak_kind": peak_kind,
                          "traffic": ncu_traffic("k_unpermute", f"{name}-T{T}")},
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "steps": n_e2e},
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4), "steps": n_e2e,
+                    "schedule": "pipelined: step i+1's host-to-device copy overlaps step i's "
+                                "kernels and device-to-host copy (two device buffer sets, "
+                                "separate copy and compute streams)",
+                    "serial_ms_per_step": round(e2e_serial_ms, 4),
+                    "serial_value": round(job_gbs(world, step_bytes, e2e_serial_ms), 1)},
             "gpu_launches": n * launches_per_step,
             "per_op_timing": "second pass of the same steps with CUDA events around each call",
             "clocks": clk.summary(),
         }
-    del h_hidden, h_rows
+    del e2e  # frees the pinned host copies before the sweep
     if rank == 0 and world == 1:
         flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
         if not args.no_sweep:
