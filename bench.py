@@ -454,6 +454,7 @@ def sweep(dev, peak, flush):
         if name == "tiny":
             continue
         for T in wl.T_sweep:
+            torch.cuda.nvtx.range_push(f"sweep {name} T={T}")
             first = Setup(name, T, seed=0, dev=dev)
             fp = first.footprint()
             n_sets = int(min(64, max(2, -(-3 * L2_BYTES // max(fp, 1)))))
@@ -494,6 +495,7 @@ def sweep(dev, peak, flush):
             rows.append(rec)
             del sets, first, s0
             torch.cuda.empty_cache()
+            torch.cuda.nvtx.range_pop()
     return rows
 
 
@@ -643,7 +645,7 @@ def main():
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(dev.index) as clk, torch.cuda.nvtx.range("timed steps"):
         start.record()
         for i in range(n):
             step(i)
@@ -674,8 +676,10 @@ def main():
     # end to end: pinned host inputs in, result out, every step
     n_e2e = min(n, 50)
     e2e = EndToEnd(sets, do_permute, args.quant)
-    e2e_serial_ms = max_over_ranks(e2e.serial_ms(n_e2e), dist, dev)
-    e2e_ms = max_over_ranks(e2e.pipelined_ms(n_e2e), dist, dev)
+    with torch.cuda.nvtx.range("end to end, serial"):
+        e2e_serial_ms = max_over_ranks(e2e.serial_ms(n_e2e), dist, dev)
+    with torch.cuda.nvtx.range("end to end, pipelined"):
+        e2e_ms = max_over_ranks(e2e.pipelined_ms(n_e2e), dist, dev)
     e2e_value = job_gbs(world, step_bytes, e2e_ms)
     h2d, d2h = e2e.h2d, e2e.d2h
 
