@@ -135,6 +135,11 @@ size_t workspace_bytes_for(int64_t max_tokens, int32_t topk, int32_t num_experts
 }
 
 constexpr int kFusedV = 4;   // vectors per lane in one gather chunk (fused kernel)
+// Same, fused kernel with its quantising copy: one vector of 8 values per
+// lane (two 128-column groups per item).  The arithmetic per item is long, so
+// more, smaller items spread it over more warps: at DeepSeek-V3 shapes on
+// GB300, T=1 4.0 us instead of 7.0 with 4 vectors, T=128 7.2 instead of 9.9.
+constexpr int kFusedQuantV = 1;
 constexpr int kGatherV = 8;  // same, gather kernel of the large-batch path
 constexpr int64_t kFusedMaxRows = 2048;  // R above this: routing grid + gather
 
@@ -368,7 +373,8 @@ cudaError_t permute_batched_typed(const IdT* ids, const int32_t* emap, int64_t T
                            &static_cast<WsHeader*>(ws)->status, d, s);
 }
 
-constexpr int kQuantV = 4;  // vectors of 8 bf16 per lane in one quantise item (8 groups)
+constexpr int kQuantV = 2;  // vectors of 8 bf16 per lane in one quantise item (4 groups);
+                            // measured 0.3-6% faster than 4 on GB300, 1 is 3-10% slower
 
 template <typename IdT>
 cudaError_t permute_quant_typed(const IdT* ids, const int32_t* emap, int64_t T, int K, int E,
@@ -376,9 +382,10 @@ cudaError_t permute_quant_typed(const IdT* ids, const int32_t* emap, int64_t T, 
                                 float* scales, int64_t* offsets, int32_t* pidx, int32_t* inv,
                                 void* ws, const DeviceInfo* d, cudaStream_t s) {
   if (T * K <= kFusedMaxRows)
-    return launch_fused<IdT, uint4, kFusedV, true>(ids, emap, T, K, E, E_local, hidden, H * 2,
-                                                   nullptr, 0, codes, scales, offsets, pidx, inv,
-                                                   static_cast<WsHeader*>(ws), d, s);
+    return launch_fused<IdT, uint4, kFusedQuantV, true>(ids, emap, T, K, E, E_local, hidden,
+                                                        H * 2, nullptr, 0, codes, scales,
+                                                        offsets, pidx, inv,
+                                                        static_cast<WsHeader*>(ws), d, s);
   cudaError_t err = launch_route<IdT>(ids, emap, T, K, E, E_local, offsets, pidx, inv,
                                       static_cast<WsHeader*>(ws), d, s);
   if (err != cudaSuccess) return err;
