@@ -105,9 +105,10 @@ MOE_API const char *moe_status_string(int status);
  * with at most `max_tokens` tokens needs, for `topk` and `num_experts` (global
  * experts).  Returns 0 for invalid arguments (max_tokens < 0, topk < 1 or
  * > MOE_MAX_TOPK, num_experts < 1, or max_tokens*topk > INT32_MAX).
- * The workspace holds the per-block expert histograms of one call, the
- * grid-barrier words and the status word.  (Digest of vLLM PR #43014, "implementation breakdown"
- * item 3: the sort workspace is sized by a query op and pre-allocated.)
+ * The workspace holds the per-block expert histograms of one call (a table
+ * whose entries carry a per-call tag), a call counter and the status word.
+ * (Digest of vLLM PR #43014, "implementation breakdown" item 3: the sort
+ * workspace is sized by a query op and pre-allocated.)
  */
 MOE_API size_t moe_permute_workspace_size(int64_t max_tokens, int32_t topk,
                                   int32_t num_experts);
