@@ -9,6 +9,7 @@ import torch
 import moe_token_permute_gb300 as mp
 import oracle
 from gpu_util import alloc_outputs, assert_metadata_equal, bits16, bytes_of
+from test_edges_gpu import custom_inputs
 from moe_token_permute_gb300.workloads import WORKLOADS, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -137,3 +138,42 @@ def test_quant_permute_zero_tokens():
     mp.moe_permute_quant_fp8(h, inp["topk_ids"].cuda(), bufs["offsets"], bufs["pidx"], bufs["inv"],
                              bufs["ws"], c, s, num_experts=wl.E)
     assert bufs["offsets"].cpu().tolist() == [0] * (wl.E + 1)
+
+
+def every_bf16_up_to(amax_bits):
+    """Bit patterns of every finite bf16 value v with |v| <= the value of amax_bits."""
+    mags = np.arange(0, 0x7F81, dtype=np.uint16)  # +0 .. +inf (exclusive of NaN)
+    mags = mags[(mags <= amax_bits) & (mags < 0x7F80)]
+    return np.concatenate([mags, mags | np.uint16(0x8000)])
+
+
+# Group maxima (bf16 bits): 448 gives scale 1 (every e4m3 midpoint is hit exactly), powers of
+# two, odd mantissas, the smallest subnormal and normal, and the largest finite bf16.
+AMAX_BITS = [0x43E0, 0x3F80, 0x4040, 0x3F95, 0x4321, 0x0001, 0x0080, 0x0C00, 0x3000, 0x3C80,
+             0x447F, 0x4B00, 0x5F00, 0x7F7F, 0x41C8, 0x3A83]
+
+
+def test_quant_every_bf16_value_against_oracle():
+    """Every finite bf16 value, under each group maximum above, quantised by the
+    kernel (multiply by the reciprocal where it provably gives the IEEE
+    quotient's code, the division elsewhere) against the oracle's division."""
+    H = 1024
+    groups = []
+    for a in AMAX_BITS:
+        vals = every_bf16_up_to(a)
+        per = G - 1
+        for i in range(0, len(vals), per):
+            g = np.full(G, a, dtype=np.uint16)  # the maximum itself, then values <= it
+            chunk = vals[i:i + per]
+            g[1:1 + len(chunk)] = chunk
+            groups.append(g)
+    while len(groups) % (H // G):
+        groups.append(np.zeros(G, dtype=np.uint16))
+    bits = np.concatenate(groups).reshape(-1, H)
+    T = bits.shape[0]
+    hidden = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16)
+    inp = custom_inputs(T, 1, 1, H, ids=torch.zeros(T, 1, dtype=torch.int32), seed=0)
+    ref = oracle_quant_permute(hidden, inp)
+    bufs, codes, scales = run_quant(hidden, inp)
+    np.testing.assert_array_equal(bytes_of(codes), ref["permuted_hidden"])
+    np.testing.assert_array_equal(scales.cpu().numpy(), ref["permuted_scales"])
