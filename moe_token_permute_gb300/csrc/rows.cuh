@@ -56,20 +56,42 @@ __device__ __forceinline__ void store_chunk(const VecT (&v)[V], VecT* __restrict
   }
 }
 
-// Copy one token's fp32 scale row (scale_cols floats) to its destinations.
-__device__ __forceinline__ void copy_token_scales(const float* __restrict__ src, int64_t scale_cols,
-                                                  float* __restrict__ out, int p_lane,
-                                                  unsigned valid) {
+// A token's first 64 scale columns, loaded ahead of its row stores so that the
+// load is not a second round trip after them (lane l holds columns l and
+// l + 32).  store_token_scales writes them, and loads and writes any further
+// columns itself.
+constexpr int kPreScaleChunks = 2;
+
+__device__ __forceinline__ void load_token_scales(const float* __restrict__ src,
+                                                  int64_t scale_cols,
+                                                  float (&s)[kPreScaleChunks]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int i = 0; i < kPreScaleChunks; ++i) {
+    const int64_t c = i * 32 + lane;
+    s[i] = c < scale_cols ? __ldg(src + c) : 0.f;
+  }
+}
+
+__device__ __forceinline__ void store_token_scales(const float* __restrict__ src,
+                                                   int64_t scale_cols,
+                                                   const float (&s)[kPreScaleChunks],
+                                                   float* __restrict__ out, int p_lane,
+                                                   unsigned valid) {
+  static_assert(kPreScaleChunks == 2, "the selection below names both preloaded chunks");
   const int lane = threadIdx.x & 31;
   for (int64_t c0 = 0; c0 < scale_cols; c0 += 32) {
     const int64_t c = c0 + lane;
-    const float s = c < scale_cols ? __ldg(src + c) : 0.f;
+    float v;
+    if (c0 == 0) v = s[0];
+    else if (c0 == 32) v = s[1];
+    else v = c < scale_cols ? __ldg(src + c) : 0.f;
     unsigned m = valid;
     while (m != 0u) {
       const int k = __ffs(m) - 1;
       m &= m - 1u;
       const int pk = __shfl_sync(kFullMask, p_lane, k);
-      if (c < scale_cols) out[static_cast<int64_t>(pk) * scale_cols + c] = s;
+      if (c < scale_cols) out[static_cast<int64_t>(pk) * scale_cols + c] = v;
     }
   }
 }
@@ -96,6 +118,9 @@ k_gather_rows(const VecT* __restrict__ hidden, int64_t row_vecs,
   const int64_t c0 = (item - t * n_chunks) * kChunk;
   VecT v[V];
   load_chunk<VecT, V>(hidden + t * row_vecs, c0, row_vecs, v);
+  const bool with_scales = permuted_scales != nullptr && c0 == 0;
+  float sc[kPreScaleChunks];
+  if (with_scales) load_token_scales(scales + t * scale_cols, scale_cols, sc);
   pdl_wait();
   int p = lane < K ? __ldcg(inv_permuted_idx + t * K + lane) : -1;
   // Positions outside [0, num_out_rows) can only come from a routing grid that
@@ -104,8 +129,25 @@ k_gather_rows(const VecT* __restrict__ hidden, int64_t row_vecs,
   const unsigned valid = __ballot_sync(kFullMask, p >= 0);
   if (valid == 0u) return;  // every row of this token was dropped
   store_chunk<VecT, V>(v, permuted_hidden, c0, row_vecs, p, valid);
-  if (permuted_scales != nullptr && c0 == 0)
-    copy_token_scales(scales + t * scale_cols, scale_cols, permuted_scales, p, valid);
+  if (with_scales)
+    store_token_scales(scales + t * scale_cols, scale_cols, sc, permuted_scales, p, valid);
+}
+
+// One item's row chunk; the quantising copy zero-fills past the row's end so
+// every lane's group maximum is defined.
+template <bool kQuant, typename VecT, int V>
+__device__ __forceinline__ void load_item(const VecT* __restrict__ src, int64_t c0,
+                                          int64_t row_vecs, VecT (&v)[V]) {
+  if constexpr (kQuant) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int64_t c = c0 + i * 32 + lane;
+      v[i] = c < row_vecs ? ld_stream(src + c) : make_uint4(0, 0, 0, 0);
+    }
+  } else {
+    load_chunk<VecT, V>(src, c0, row_vecs, v);
+  }
 }
 
 // Single-launch permute for small batches (R <= kMetaChunkRows expanded rows).  Every block
@@ -189,7 +231,10 @@ k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
   __syncthreads();
 
   // Items go round-robin over the blocks first (item i -> block i % G), so a
-  // small batch still spreads its copy over every block's SM.
+  // small batch still spreads its copy over every block's SM.  A token's
+  // scales are loaded with its first row chunk, before any store.  (Loading
+  // each warp's first chunk before the ranking, to overlap the two, measured
+  // 0.2 us slower at T = 1 even when switched off at run time.)
   constexpr int64_t kChunk = 32 * V;
   const int64_t n_chunks = (row_vecs + kChunk - 1) / kChunk;
   const int64_t n_items = T * n_chunks;
@@ -200,20 +245,18 @@ k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
     const int p = lane < K ? s_p[t * K + lane] : -1;
     const unsigned valid = __ballot_sync(kFullMask, p >= 0);
     if (valid == 0u) continue;
+    const bool with_scales = !kQuant && permuted_scales != nullptr && c0 == 0;
     VecT v[V];
+    float sc[kPreScaleChunks];
+    load_item<kQuant, VecT, V>(hidden + t * row_vecs, c0, row_vecs, v);
+    if (with_scales) load_token_scales(scales + t * scale_cols, scale_cols, sc);
     if constexpr (kQuant) {
-#pragma unroll
-      for (int i = 0; i < V; ++i) {
-        const int64_t c = c0 + i * 32 + lane;
-        v[i] = c < row_vecs ? ld_stream(hidden + t * row_vecs + c) : make_uint4(0, 0, 0, 0);
-      }
       quant_store_chunk<V>(v, c0, row_vecs, p, valid, reinterpret_cast<uint2*>(permuted_hidden),
                            permuted_scales);
     } else {
-      load_chunk<VecT, V>(hidden + t * row_vecs, c0, row_vecs, v);
       store_chunk<VecT, V>(v, permuted_hidden, c0, row_vecs, p, valid);
-      if (permuted_scales != nullptr && c0 == 0)
-        copy_token_scales(scales + t * scale_cols, scale_cols, permuted_scales, p, valid);
+      if (with_scales)
+        store_token_scales(scales + t * scale_cols, scale_cols, sc, permuted_scales, p, valid);
     }
   }
 }
