@@ -158,6 +158,11 @@ k_gather_rows_tma(const char* __restrict__ hidden, int64_t row_bytes, int64_t ch
     const int64_t t = item / n_chunks;
     const int64_t c0 = (item - t * n_chunks) * chunk_bytes;
     const uint32_t bytes = static_cast<uint32_t>(min(chunk_bytes, row_bytes - c0));
+    // The token's scales are loaded before the wait for its row, so the load
+    // is not a second round trip after the stores.
+    const bool with_scales = out_scales != nullptr && c0 == 0;
+    float sc[kPreScaleChunks];
+    if (with_scales) load_token_scales(scales + t * scale_cols, scale_cols, sc);
     int p = lane < K ? __ldcg(inv_permuted_idx + t * K + lane) : -1;
     if (p >= num_out_rows) p = -1;  // only a routing grid that gave up leaves such values
     const unsigned valid = __ballot_sync(kFullMask, p >= 0);
@@ -185,19 +190,8 @@ k_gather_rows_tma(const char* __restrict__ hidden, int64_t row_bytes, int64_t ch
       if (lane == 0) bulk_store(out + static_cast<int64_t>(pk) * row_bytes + c0, stages + s * pitch, bytes);
     }
     if (lane == 0) bulk_commit();
-    if (out_scales != nullptr && c0 == 0 && valid != 0u) {
-      for (int64_t c1 = 0; c1 < scale_cols; c1 += 32) {
-        const int64_t c = c1 + lane;
-        const float v = c < scale_cols ? __ldg(scales + t * scale_cols + c) : 0.f;
-        unsigned mm = valid;
-        while (mm != 0u) {
-          const int k = __ffs(mm) - 1;
-          mm &= mm - 1u;
-          const int pk = __shfl_sync(kFullMask, p, k);
-          if (c < scale_cols) out_scales[static_cast<int64_t>(pk) * scale_cols + c] = v;
-        }
-      }
-    }
+    if (with_scales && valid != 0u)
+      store_token_scales(scales + t * scale_cols, scale_cols, sc, out_scales, p, valid);
     // Refill this stage with the item kTmaStages steps ahead once the stores
     // just issued have read it.
     const int64_t next = item + kTmaStages * n_gw;

@@ -56,46 +56,6 @@ __device__ __forceinline__ void store_chunk(const VecT (&v)[V], VecT* __restrict
   }
 }
 
-// A token's first 64 scale columns, loaded ahead of its row stores so that the
-// load is not a second round trip after them (lane l holds columns l and
-// l + 32).  store_token_scales writes them, and loads and writes any further
-// columns itself.
-constexpr int kPreScaleChunks = 2;
-
-__device__ __forceinline__ void load_token_scales(const float* __restrict__ src,
-                                                  int64_t scale_cols,
-                                                  float (&s)[kPreScaleChunks]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int i = 0; i < kPreScaleChunks; ++i) {
-    const int64_t c = i * 32 + lane;
-    s[i] = c < scale_cols ? __ldg(src + c) : 0.f;
-  }
-}
-
-__device__ __forceinline__ void store_token_scales(const float* __restrict__ src,
-                                                   int64_t scale_cols,
-                                                   const float (&s)[kPreScaleChunks],
-                                                   float* __restrict__ out, int p_lane,
-                                                   unsigned valid) {
-  static_assert(kPreScaleChunks == 2, "the selection below names both preloaded chunks");
-  const int lane = threadIdx.x & 31;
-  for (int64_t c0 = 0; c0 < scale_cols; c0 += 32) {
-    const int64_t c = c0 + lane;
-    float v;
-    if (c0 == 0) v = s[0];
-    else if (c0 == 32) v = s[1];
-    else v = c < scale_cols ? __ldg(src + c) : 0.f;
-    unsigned m = valid;
-    while (m != 0u) {
-      const int k = __ffs(m) - 1;
-      m &= m - 1u;
-      const int pk = __shfl_sync(kFullMask, p_lane, k);
-      if (c < scale_cols) out[static_cast<int64_t>(pk) * scale_cols + c] = v;
-    }
-  }
-}
-
 // Row gather of the large-batch permute: one warp per (token, chunk) item, one
 // item per warp, so the hardware block scheduler balances the work across SMs.
 // Launched as the dependent of the routing grid, which lets it start early:
