@@ -301,12 +301,16 @@ double writes_per_row(int K, int E, int E_local, const int32_t* emap) {
 // it beats the register gather.  The bulk-copy gather loads most rows while
 // routing runs, but its stores of each chunk come from one warp; the register
 // gather keeps more stores in flight.  So the crossover falls as the rows
-// written per source row grow (measured on GB300: about 2x at 1-2 writes per
-// row, 1.1-1.25x at 8, the lower end for 4 KB rows, which the register
-// gather moves in whole chunks).  writes_per_row: K, or K * E_local / E with
-// an expert map (uniform routing).
-double tma_max_ratio(double writes_per_row) {
-  return std::min(2.0, std::max(1.15, 2.0 - (writes_per_row - 2.0) * 0.85 / 6.0));
+// written per source row grow: measured on GB300, about 2x at 1-2 writes per
+// row, and at 8 about 1.05x for rows the register gather moves in whole
+// 16-byte-vector chunks (a multiple of 32 * kGatherV vectors, e.g. 4 KB), but
+// 1.25x for rows it splits raggedly (e.g. 7168 bytes: a 4 KB and a 3 KB
+// chunk).  writes_per_row: K, or K * E_local / E with an expert map (uniform
+// routing).
+double tma_max_ratio(double writes_per_row, int64_t row_bytes) {
+  const bool whole_chunks = row_bytes % (32 * kGatherV * 16) == 0;
+  const double at8 = whole_chunks ? 1.05 : 1.25;
+  return std::min(2.0, std::max(at8, 2.0 - (writes_per_row - 2.0) * (2.0 - at8) / 6.0));
 }
 
 // The row gather for any vector width: out rows are indexed by inv values in
@@ -319,7 +323,7 @@ cudaError_t launch_gather_any(size_t vb, const void* hidden, int64_t row_bytes,
                               float* out_scales, int64_t num_out_rows, unsigned* status,
                               const DeviceInfo* d, cudaStream_t s) {
   if (vb == 16 && static_cast<double>(T * row_bytes) <=
-                      tma_max_ratio(writes_per_row) *
+                      tma_max_ratio(writes_per_row, row_bytes) *
                           static_cast<double>(tma_geometry(row_bytes, T, d).prefetch_bytes))
     return launch_gather_tma(hidden, row_bytes, scales, scale_cols, inv, T, K, out, out_scales,
                              num_out_rows, status, d, s);
