@@ -329,14 +329,19 @@ class EndToEnd:
         self.h_out[1].copy_(st.offsets, non_blocking=True)
 
     @staticmethod
-    def _timed(fn, n):
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        fn(n)
-        b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / n
+    def _timed(fn, n, reps=3):
+        """Median over `reps` timed runs of n steps (ms per step): one stall of
+        the shared host or link does not decide the number."""
+        times = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn(n)
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b) / n)
+        return statistics.median(times)
 
     def serial_ms(self, n):
         def run(k):
@@ -352,16 +357,18 @@ class EndToEnd:
         s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
         n_sets = len(self.sets)
 
+        start = torch.cuda.Event()
+        in_done = [torch.cuda.Event() for _ in range(n_sets)]
+        cmp_done = [torch.cuda.Event() for _ in range(n_sets)]
+        out_done = [torch.cuda.Event() for _ in range(n_sets)]
+
         def run(k):
-            start = torch.cuda.Event()
             start.record(cur)
             for st in (s_in, s_cmp, s_out):
                 st.wait_event(start)
-            in_done = [torch.cuda.Event() for _ in range(n_sets)]
-            out_done = [None] * n_sets
             for i in range(k):
                 j = i % n_sets
-                if out_done[j] is not None:
+                if i >= n_sets:
                     s_in.wait_event(out_done[j])  # set j's previous step is fully done
                 with torch.cuda.stream(s_in):
                     self._copy_in(j)
@@ -369,12 +376,10 @@ class EndToEnd:
                 s_cmp.wait_event(in_done[j])
                 with torch.cuda.stream(s_cmp):
                     self._compute(j)
-                cmp_done = torch.cuda.Event()
-                cmp_done.record(s_cmp)
-                s_out.wait_event(cmp_done)
+                cmp_done[j].record(s_cmp)
+                s_out.wait_event(cmp_done[j])
                 with torch.cuda.stream(s_out):
                     self._copy_out(j)
-                out_done[j] = torch.cuda.Event()
                 out_done[j].record(s_out)
             for st in (s_in, s_cmp, s_out):
                 cur.wait_stream(st)
@@ -718,6 +723,7 @@ def main():
                     "schedule": "pipelined: step i+1's host-to-device copy overlaps step i's "
                                 "kernels and device-to-host copy (two device buffer sets, "
                                 "separate copy and compute streams)",
+                    "timing": "median of 3 timed runs of `steps` steps, each schedule",
                     "serial_ms_per_step": round(e2e_serial_ms, 4),
                     "serial_value": round(job_gbs(world, step_bytes, e2e_serial_ms), 1)},
             "gpu_launches": n * launches_per_step,

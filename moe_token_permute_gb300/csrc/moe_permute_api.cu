@@ -234,7 +234,7 @@ cudaError_t launch_route(const IdT* ids, const int32_t* emap, int64_t T, int K, 
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;  // all blocks co-resident (grid barrier)
+  attr[0].id = cudaLaunchAttributeCooperative;  // all blocks co-resident (each waits for the others' table rows)
   attr[0].val.cooperative = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
