@@ -11,7 +11,7 @@
 // rows [r0, r1).  Phases:
 //   1. histogram of the block's rows -> row b of the table (workspace), each
 //      entry tagged with this call's tag.  When the block's rows fit one
-//      round (kRouteRoundRows), the stable in-block ranks are computed in the
+//      round (kRouteThreads * J rows), the stable in-block ranks are computed in the
 //      same pass and kept in registers;
 //   2. every block reads the whole [B][E_local] table with 16-byte loads,
 //      re-reading entries that do not carry this call's tag yet (every block
@@ -44,8 +44,10 @@ namespace moe {
 
 constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / kWarpSize;
+// Rows per lane in one round (J): 4 (1024 rows per round) normally; 8, with
+// half the blocks, when the [B][E] table every block reads is large.
 constexpr int kRouteRowsPerLane = 4;
-constexpr int kRouteRoundRows = kRouteThreads * kRouteRowsPerLane;  // 1024
+constexpr int kRouteRowsPerLaneLargeTable = 8;
 constexpr unsigned kTablePollLimit = 1u << 24;                   // polls before giving up
 constexpr unsigned long long kTableTimeLimitNs = 2000000000ull;  // or 2 s, whichever first
 constexpr int kTagShift = 24;
@@ -154,7 +156,7 @@ __device__ __forceinline__ int place_row(int p, int e, int64_t r, int64_t M, con
 // rows with j >= M are dropped (MOE_FLAG_CAPACITY_OVERFLOW).  Block 0 writes
 // expert_num_tokens[e] = min(rows of e, M); offsets and permuted_idx are not
 // used.
-template <typename IdT>
+template <typename IdT, int J>
 __global__ void __launch_bounds__(kRouteThreads, 4)
 k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
              int64_t T, int K, int E, int E_local,
@@ -178,8 +180,8 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
   const int64_t t0 = min(T, static_cast<int64_t>(b) * tpb);
   const int64_t t1 = min(T, t0 + tpb);
   const int64_t r0 = t0 * K, r1 = t1 * K;
-  const bool one_round = r1 - r0 <= kRouteRoundRows;
-  constexpr int J = kRouteRowsPerLane;
+  constexpr int kRoundRows = kRouteThreads * J;
+  const bool one_round = r1 - r0 <= kRoundRows;
 
   pdl_wait();
   pdl_launch_dependents();
@@ -342,8 +344,8 @@ k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
   // More rows than one round: rank round by round; s_run[e] = this block's
   // rows of expert e placed so far.
   for (int e = threadIdx.x; e < E_local; e += blockDim.x) s_run[e] = 0;
-  for (int64_t q0 = r0; q0 < r1; q0 += kRouteRoundRows) {
-    const int64_t q1 = min(r1, q0 + kRouteRoundRows);
+  for (int64_t q0 = r0; q0 < r1; q0 += kRoundRows) {
+    const int64_t q1 = min(r1, q0 + kRoundRows);
     for (int i = threadIdx.x; i < kRouteWarps * E_local; i += blockDim.x) cnt[i] = 0;
     __syncthreads();
     const int64_t s0 = q0 + static_cast<int64_t>(warp) * 32 * J;

@@ -26,10 +26,11 @@ def shared_workspace(shapes):
     return ws
 
 
-# (workload, T, with rows): table extents 128x128, 8x8, 64x256, 18x16, 128x128, 59x8, 1x8
+# (workload, T, with rows): table extents 128x128, 8x8, 64x256, 79x256 (a large table:
+# rounds of 8 rows per lane), 18x16, 128x128, 59x8, 1x8
 SEQUENCE = [("qwen3", 16384, False), ("mixtral", 4096, True), ("dsv3", 8192, False),
-            ("dsv2lite", 3000, True), ("qwen3", 16384, False), ("mixtral", 30000, False),
-            ("mixtral", 1024, True), ("qwen3", 5000, True)]
+            ("dsv3", 20000, False), ("dsv2lite", 3000, True), ("qwen3", 16384, False),
+            ("mixtral", 30000, False), ("mixtral", 1024, True), ("qwen3", 5000, True)]
 
 
 def test_shapes_growing_and_shrinking_share_one_workspace():
