@@ -79,3 +79,49 @@ def test_more_calls_than_tags():
             bad.append(i)
     assert bad == []
     assert mp.moe_read_status(ws) == 0
+
+
+def test_graph_replays_alternating_on_one_workspace():
+    """Two CUDA graphs (different shapes, so different table extents) captured
+    on one workspace and replayed alternately 150 times: each replay takes its
+    table tag from the workspace, not from the captured arguments, so every
+    replay's metadata must match the oracle."""
+    a = make_inputs("qwen3", 3000, seed=31, with_rows=False)
+    b = make_inputs("dsv3", 6000, seed=32, with_rows=False)
+    ws = shared_workspace([(x["T"], x["wl"].K, x["wl"].E) for x in (a, b)])
+    cases = []
+    for inp in (a, b):
+        wl = inp["wl"]
+        ref = oracle_route(inp)
+        bufs = alloc_outputs(inp["T"], wl.K, wl.e_local, E=wl.E)
+        bufs["ws"] = ws
+        ids = inp["topk_ids"].cuda()
+        expect = {k: torch.from_numpy(ref[v]).cuda() for k, v in
+                  (("offsets", "offsets"), ("pidx", "permuted_idx"), ("inv", "inv_permuted_idx"))}
+
+        def call(ids=ids, bufs=bufs, wl=wl):
+            mp.moe_permute(None, ids, bufs["offsets"], bufs["pidx"], bufs["inv"], bufs["ws"],
+                           num_experts=wl.E, num_local_experts=wl.e_local)
+
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            call()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call()
+        # the graph reads ids by address: keep the tensor (and the closure) alive
+        cases.append((g, bufs, expect, ids, call))
+    bad = []
+    for i in range(150):
+        g, bufs, expect, _, _ = cases[i % 2]
+        for k in expect:
+            bufs[k].fill_(-5)
+        g.replay()
+        torch.cuda.synchronize()
+        if not all(torch.equal(bufs[k], expect[k]) for k in expect):
+            bad.append(i)
+    assert bad == []
+    assert mp.moe_read_status(ws) == 0
