@@ -117,3 +117,17 @@ def test_batched_zero_tokens():
     inp = make_inputs("qwen3", 0, seed=1, with_rows=False)
     got = run_batched(inp, 4, metadata_only=True)
     assert got["counts"].cpu().tolist() == [0] * inp["wl"].E
+
+
+def test_batched_metadata_only_large_table():
+    """256 local experts at T = 20000: the routing grid's histogram table would
+    reach 152 x 256 entries, so it runs rounds of 8 rows per lane over half the
+    blocks; the batched slot map and counts must still match the oracle."""
+    inp = make_inputs("dsv3", 20000, seed=8, with_rows=False)
+    wl = inp["wl"]
+    M = 512  # popular experts overflow: rows past the capacity are dropped and flagged
+    got = run_batched(inp, M, metadata_only=True)
+    ref = oracle.permute_batched(inp["topk_ids"].cpu().numpy(), wl.E, M)
+    np.testing.assert_array_equal(got["counts"].cpu().numpy(), ref["expert_num_tokens"])
+    np.testing.assert_array_equal(got["inv"].cpu().numpy(), ref["inv_permuted_idx"])
+    assert mp.moe_read_status(got["ws"]) == ref["flags"]
