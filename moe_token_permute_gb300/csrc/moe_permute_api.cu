@@ -143,6 +143,7 @@ constexpr int kFusedV = 4;   // vectors per lane in one gather chunk (fused kern
 constexpr int kFusedQuantV = 1;
 constexpr int kGatherV = 8;  // same, gather kernel of the large-batch path
 constexpr int64_t kFusedMaxRows = 2048;  // R above this: routing grid + gather
+static_assert(kFusedMaxRows <= kMetaChunkRows, "one block must be able to rank every row");
 
 // (token, chunk) work items of a row kernel.
 int64_t row_items(int64_t T, int64_t row_vecs, int V) {

@@ -110,8 +110,8 @@ __device__ __forceinline__ void load_item(const VecT* __restrict__ src, int64_t 
   }
 }
 
-// Single-launch permute for small batches (at most kMetaChunkRows expanded rows; the
-// host uses it up to 2048, where it measured faster than the two-kernel path).  Every block
+// Single-launch permute for small batches (at most kMetaChunkRows = 2048 expanded rows,
+// where it measured faster than the two-kernel path).  Every block
 // computes the whole stable counting sort in shared memory (R is small, the
 // ids come from L2), block 0 writes the metadata, and all blocks share the
 // row copy: no block ever waits for another.

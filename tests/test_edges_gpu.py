@@ -122,6 +122,13 @@ def test_max_topk_and_max_local_experts(T):
     check_case(custom_inputs(T, K, E, 64, seed=5))
 
 
+@pytest.mark.parametrize("T,K", [(256, 8), (2048, 1), (1, 32)])
+def test_single_launch_with_max_local_experts(T, K):
+    """Up to 2048 rows over 1024 experts in one launch: every warp ranks, and
+    the per-warp counts take [32][1024] ints of shared memory."""
+    check_case(custom_inputs(T, K, mp.MOE_MAX_LOCAL_EXPERTS, 64, seed=T + K))
+
+
 @pytest.mark.parametrize("T", [700, 9000])
 def test_expert_map_with_max_local_experts(T):
     E, EL = 2048, 1024
