@@ -214,8 +214,9 @@ cudaError_t launch_route(const IdT* ids, const int32_t* emap, int64_t T, int K, 
   // block reads is [B][E_pad], and the rest of each SM stays free for the
   // gather blocks that start while routing runs.  When that table reaches
   // kLargeTable entries (e.g. 152 blocks x 256 experts), reading it dominates:
-  // rounds of 8 rows per lane halve the blocks (measured on GB300: DeepSeek-V3
-  // T = 32768 permute 2.2% faster; smaller tables were up to 6% slower).
+  // rounds of twice the rows per lane halve the blocks (measured on GB300:
+  // DeepSeek-V3 T = 32768 permute 2.2% faster; smaller tables were up to 6%
+  // slower).
   const int64_t e_pad = (E_local + 3) / 4 * 4;
   int J = kRouteRowsPerLane;
   int64_t B = std::min<int64_t>(ceil_div(T, std::max<int64_t>(1, kRouteThreads * J / K)),

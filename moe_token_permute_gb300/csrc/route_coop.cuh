@@ -42,12 +42,15 @@
 
 namespace moe {
 
-constexpr int kRouteThreads = 256;
+// 512 threads x 2 rows per lane: 1024 rows per round, with short per-lane
+// ranking loops and twice the threads for reading the table (measured on
+// GB300 against 256 x 4: permute 0.4-2.9% faster on every workload shape).
+constexpr int kRouteThreads = 512;
 constexpr int kRouteWarps = kRouteThreads / kWarpSize;
-// Rows per lane in one round (J): 4 (1024 rows per round) normally; 8, with
+// Rows per lane in one round (J): 2 (1024 rows per round) normally; 4, with
 // half the blocks, when the [B][E] table every block reads is large.
-constexpr int kRouteRowsPerLane = 4;
-constexpr int kRouteRowsPerLaneLargeTable = 8;
+constexpr int kRouteRowsPerLane = 2;
+constexpr int kRouteRowsPerLaneLargeTable = 4;
 constexpr unsigned kTablePollLimit = 1u << 24;                   // polls before giving up
 constexpr unsigned long long kTableTimeLimitNs = 2000000000ull;  // or 2 s, whichever first
 constexpr int kTagShift = 24;
@@ -157,7 +160,7 @@ __device__ __forceinline__ int place_row(int p, int e, int64_t r, int64_t M, con
 // expert_num_tokens[e] = min(rows of e, M); offsets and permuted_idx are not
 // used.
 template <typename IdT, int J>
-__global__ void __launch_bounds__(kRouteThreads, 4)
+__global__ void __launch_bounds__(kRouteThreads, 2)
 k_route_coop(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
              int64_t T, int K, int E, int E_local,
              int64_t* __restrict__ offsets, int32_t* __restrict__ permuted_idx,
