@@ -449,7 +449,8 @@ def sweep(dev, peak, flush):
     enough buffer sets that the footprint is at least 3x the L2 size (or 64
     sets for the smallest batches).  *_us is the device time per call from
     replaying a CUDA graph of back-to-back calls (no Python launch cost);
-    *_eager_us the same calls launched one by one from Python; at T = 1 also a
+    *_eager_us the same calls launched one by one from Python (1000 of them
+    up to 64 tokens); at T = 1 also a
     single eager call after an L2 flush.  metadata_permute_us: the routing
     metadata alone (no row gather), a latency workload.  For the DeepSeek-V3 shape also
     quantise-on-permute from bf16 rows (quant_fp8_permute_*); for the Qwen3
@@ -464,7 +465,7 @@ def sweep(dev, peak, flush):
             fp = first.footprint()
             n_sets = int(min(64, max(2, -(-3 * L2_BYTES // max(fp, 1)))))
             sets = [first] + [Setup(name, T, seed=i, dev=dev) for i in range(1, n_sets)]
-            n = max(3 * n_sets, 30 if T >= 4096 else 200)
+            n = max(3 * n_sets, 30 if T >= 4096 else (1000 if T <= 64 else 200))
             n_graph = max(n_sets, 20 if T >= 4096 else 100)
             p_us = graph_us([s.permute for s in sets], n_graph)
             u_us = graph_us([s.unpermute for s in sets], n_graph)
