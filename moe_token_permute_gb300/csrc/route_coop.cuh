@@ -121,7 +121,8 @@ __device__ __forceinline__ bool poll_quad(const unsigned* p, unsigned tag, uint4
 // this block's row (so this read sees the old value).  Called after the
 // block's first id loads are issued, so neither round trip delays them
 // (measured on GB300 against reading gen first and the extent in the block's
-// last step: metadata-only permute 0.1-0.45 us faster, permute up to 0.3 us).
+// last step: metadata-only permute 0.2-0.55 us faster, permute unchanged to
+// 0.3 us faster).
 __device__ __forceinline__ void read_gen(const WsHeader* hdr, unsigned hi, unsigned* s_gen,
                                          unsigned* s_hi) {
   if (threadIdx.x != 0) return;
