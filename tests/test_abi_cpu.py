@@ -145,3 +145,70 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         b.lib()
+
+
+def _quant_args(**over):
+    # moe_permute_quant_fp8 with fake (never dereferenced) device pointers
+    args = dict(hidden=0x1000, ids=0x2000, idt=b.MOE_INDEX_INT32, emap=None, T=4, H=256, K=2,
+                E=4, EL=4, codes=0x3000, scales=0x8000, offsets=0x4000, pidx=0x5000,
+                inv=0x6000, ws=0x10000, ws_bytes=1 << 20, stream=None)
+    args.update(over)
+    return list(args.values())
+
+
+@pytest.mark.parametrize("over", [
+    dict(H=100), dict(H=64), dict(H=0), dict(K=0), dict(K=33), dict(E=0), dict(EL=5),
+    dict(EL=2),  # EL != E without a map
+    dict(T=-1), dict(idt=3), dict(offsets=None), dict(offsets=0x4004), dict(ids=None),
+    dict(ids=0x2002), dict(pidx=None), dict(inv=0x6002), dict(hidden=None),
+    dict(hidden=0x1008),  # bf16 rows are read in 16-byte vectors
+    dict(codes=None), dict(codes=0x3004), dict(scales=None), dict(scales=0x8002),
+    dict(ws=None), dict(ws=0x10010), dict(T=2**30, K=4),
+])
+def test_quant_permute_rejects_bad_arguments_on_host(lib, over):
+    assert lib.moe_permute_quant_fp8(*_quant_args(**over)) == b.MOE_ERR_INVALID_ARG
+
+
+def test_quant_permute_workspace_too_small(lib):
+    assert (lib.moe_permute_quant_fp8(*_quant_args(T=100000, ws_bytes=512))
+            == b.MOE_ERR_WORKSPACE_TOO_SMALL)
+
+
+def _batched_args(**over):
+    # moe_permute_batched with fake (never dereferenced) device pointers
+    args = dict(hidden=0x1000, dt=b.MOE_DTYPE_BF16, scales=None, scale_cols=0, ids=0x2000,
+                idt=b.MOE_INDEX_INT32, emap=None, T=4, H=8, K=2, E=4, EL=4, M=8, out=0x3000,
+                out_scales=None, counts=0x4000, inv=0x6000, ws=0x10000, ws_bytes=1 << 20,
+                stream=None)
+    args.update(over)
+    return list(args.values())
+
+
+@pytest.mark.parametrize("over", [
+    dict(dt=9), dict(M=0), dict(M=-3), dict(M=2**31 // 4 + 1),  # E_L * M beyond int32
+    dict(K=0), dict(K=33), dict(E=0), dict(EL=2), dict(T=-1), dict(H=0), dict(idt=3),
+    dict(counts=None), dict(counts=0x4002), dict(ids=None), dict(inv=None), dict(inv=0x6002),
+    dict(hidden=None),  # rows asked for without a source
+    dict(scales=0x8000),  # source scales without output scales
+    dict(scales=0x8000, out_scales=0x9000, scale_cols=0),
+    dict(scale_cols=2),  # a scale width without scales
+    dict(ws=None), dict(ws=0x10010),
+])
+def test_batched_permute_rejects_bad_arguments_on_host(lib, over):
+    assert lib.moe_permute_batched(*_batched_args(**over)) == b.MOE_ERR_INVALID_ARG
+
+
+def test_batched_permute_workspace_too_small(lib):
+    assert (lib.moe_permute_batched(*_batched_args(T=100000, ws_bytes=512))
+            == b.MOE_ERR_WORKSPACE_TOO_SMALL)
+
+
+def test_noalloc_rejects_problems_beyond_its_scratch_on_host(lib):
+    # 512 experts: the histogram table alone outgrows the library's fixed scratch,
+    # which the call reports before it touches a device
+    assert lib.moe_permute_workspace_size(4096, 2, 512) > b.MOE_NOALLOC_SCRATCH_BYTES
+    args = list(dict(hidden=0x1000, dt=b.MOE_DTYPE_BF16, scales=None, scale_cols=0, ids=0x2000,
+                     idt=b.MOE_INDEX_INT32, emap=None, T=4096, H=8, K=2, E=512, EL=512,
+                     out=0x3000, out_scales=None, offsets=0x4000, pidx=0x5000, inv=0x6000,
+                     stream=None).values())
+    assert lib.moe_permute_noalloc(*args) == b.MOE_ERR_WORKSPACE_TOO_SMALL
