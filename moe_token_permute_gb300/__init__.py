@@ -39,6 +39,24 @@ def _ptr(t):
     return t.data_ptr()
 
 
+def _need(t, n, what):
+    """The C entry points take bare pointers, so a buffer too small for the
+    call would be written or read out of bounds on the device: refuse it
+    here, before any pointer is taken."""
+    if t is not None and t.numel() < n:
+        raise ValueError(f"{what} holds {t.numel()} elements; this call needs {n}")
+
+
+def _need_bytes(t, n, what):
+    if t is not None and t.numel() * t.element_size() < n:
+        raise ValueError(f"{what} holds {t.numel() * t.element_size()} bytes; this call needs {n}")
+
+
+def _need_rows(t, T, what):
+    if t is not None and (t.dim() != 2 or t.shape[0] < T):
+        raise ValueError(f"{what} must be 2-D with at least {T} rows (one per token)")
+
+
 def _stream(stream):
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -81,12 +99,21 @@ def moe_permute(hidden_states, topk_ids, expert_first_token_offset, permuted_idx
     T, K = topk_ids.shape
     if num_local_experts is None:
         num_local_experts = num_experts
+    _need_rows(hidden_states, T, "hidden_states")
+    _need_rows(hidden_scales, T, "hidden_scales")
     if hidden_states is not None:
         H = hidden_states.shape[1]
         dt = _DTYPES[hidden_states.dtype]
+        _need_bytes(permuted_hidden_states, T * K * H * hidden_states.element_size(),
+                    "permuted_hidden_states")
     else:
         H, dt = 1, _b.MOE_DTYPE_BF16
     scale_cols = hidden_scales.shape[1] if hidden_scales is not None else 0
+    _need(permuted_scales, T * K * scale_cols, "permuted_scales")
+    _need(expert_first_token_offset, num_local_experts + 1, "expert_first_token_offset")
+    _need(permuted_idx, T * K, "permuted_idx")
+    _need(inv_permuted_idx, T * K, "inv_permuted_idx")
+    _need(expert_map, num_experts, "expert_map")
     _b.check("moe_permute", _b.lib().moe_permute(
         _ptr(hidden_states), dt, _ptr(hidden_scales), scale_cols,
         _ptr(topk_ids), _INDEX[topk_ids.dtype], _ptr(expert_map),
@@ -107,12 +134,21 @@ def moe_permute_batched(hidden_states, topk_ids, expert_num_tokens, inv_permuted
     T, K = topk_ids.shape
     if num_local_experts is None:
         num_local_experts = num_experts
+    slots = num_local_experts * int(max_rows_per_expert)
+    _need_rows(hidden_states, T, "hidden_states")
+    _need_rows(hidden_scales, T, "hidden_scales")
     if hidden_states is not None:
         H = hidden_states.shape[1]
         dt = _DTYPES[hidden_states.dtype]
+        _need_bytes(batched_hidden_states, slots * H * hidden_states.element_size(),
+                    "batched_hidden_states")
     else:
         H, dt = 1, _b.MOE_DTYPE_BF16
     scale_cols = hidden_scales.shape[1] if hidden_scales is not None else 0
+    _need(batched_scales, slots * scale_cols, "batched_scales")
+    _need(expert_num_tokens, num_local_experts, "expert_num_tokens")
+    _need(inv_permuted_idx, T * K, "inv_permuted_idx")
+    _need(expert_map, num_experts, "expert_map")
     _b.check("moe_permute_batched", _b.lib().moe_permute_batched(
         _ptr(hidden_states), dt, _ptr(hidden_scales), scale_cols,
         _ptr(topk_ids), _INDEX[topk_ids.dtype], _ptr(expert_map),
@@ -136,6 +172,14 @@ def moe_permute_quant_fp8(hidden_states, topk_ids, expert_first_token_offset, pe
         raise ValueError("permuted_codes must be float8_e4m3fn (or raw uint8)")
     if num_local_experts is None:
         num_local_experts = num_experts
+    _need_rows(hidden_states, T, "hidden_states")
+    H = hidden_states.shape[1]
+    _need_bytes(permuted_codes, T * K * H, "permuted_codes")
+    _need(permuted_scales, T * K * (H // _b.MOE_QUANT_GROUP), "permuted_scales")
+    _need(expert_first_token_offset, num_local_experts + 1, "expert_first_token_offset")
+    _need(permuted_idx, T * K, "permuted_idx")
+    _need(inv_permuted_idx, T * K, "inv_permuted_idx")
+    _need(expert_map, num_experts, "expert_map")
     _b.check("moe_permute_quant_fp8", _b.lib().moe_permute_quant_fp8(
         _ptr(hidden_states), _ptr(topk_ids), _INDEX[topk_ids.dtype], _ptr(expert_map),
         T, hidden_states.shape[1], K, num_experts, num_local_experts,
@@ -159,6 +203,8 @@ def moe_unpermute(permuted_rows, topk_weights, inv_permuted_idx, out, *, workspa
         raise ValueError("topk_weights must be float32 and inv_permuted_idx int32")
     if permuted_rows.shape[1] != H:
         raise ValueError("hidden size mismatch between rows and out")
+    _need_rows(out, T, "out")
+    _need(inv_permuted_idx, T * K, "inv_permuted_idx")
     _b.check("moe_unpermute", _b.lib().moe_unpermute(
         _ptr(permuted_rows), permuted_rows.shape[0], _ptr(topk_weights),
         _ptr(inv_permuted_idx), T, H, K, _ptr(out), _ptr(workspace), _stream(stream)))
