@@ -71,7 +71,7 @@ def unpermute_f32_sums(rows, w, inv, T, K, H):
             acc = 0.0
             for k in range(K):
                 p = inv[t * K + k]
-                if p < 0:
+                if p < 0 or p >= len(rows):
                     continue
                 acc = _f32(acc + _f32(_f32(w[t][k]) * rows[p][h]))
             line.append(acc)

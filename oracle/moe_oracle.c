@@ -48,10 +48,12 @@
  *    expert e go to slots e*M + j, j = the row's stable rank inside the expert,
  *    for a per-expert capacity M; rows with j >= M do not fit and are dropped
  *    with ORC_FLAG_CAPACITY; expert_num_tokens[e] = min(count, M).
- *  - Unpermute: acc = 0.0f; for k = 0..K-1 in order, if inv[t*K+k] >= 0,
- *    acc = acc + w[t,k] * float(row) (fp32 multiply, then fp32 add); the
- *    result is rounded once to bf16, round-to-nearest-even.  A token with no
- *    valid row yields +0.0.
+ *  - Unpermute: acc = 0.0f; for k = 0..K-1 in order, if inv[t*K+k] names a
+ *    row (0 <= inv < num_rows), acc = acc + w[t,k] * float(row) (fp32
+ *    multiply, then fp32 add); the result is rounded once to bf16,
+ *    round-to-nearest-even.  A token with no valid row yields +0.0.  -1 is a
+ *    dropped row; any other value outside [0, num_rows) is skipped as well
+ *    and raises ORC_FLAG_INV_RANGE.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -202,8 +204,10 @@ static uint16_t orc_f32_to_bf16_rne(float f)
 
 /*
  * oracle_unpermute: out[t] = bf16_rne( sum_k w[t,k] * rows[inv[t*K+k]] ),
- * k ascending, fp32 multiply then fp32 add, dropped rows (inv < 0) skipped.
- * An inv value >= num_rows is also skipped and raises ORC_FLAG_INV_RANGE.
+ * k ascending, fp32 multiply then fp32 add, dropped rows (inv = -1) skipped.
+ * An inv value outside [-1, num_rows) -- at or past the end of rows, or below
+ * -1 -- names no row and no dropped row: it is skipped too and raises
+ * ORC_FLAG_INV_RANGE.
  *
  * rows: [num_rows, H] bf16 bits; w: [T, K] fp32; inv: [T*K] int32;
  * out: [T, H] bf16 bits.
@@ -215,7 +219,7 @@ uint32_t oracle_unpermute(const uint16_t *rows, int64_t num_rows,
     uint32_t flags = 0;
     for (int64_t t = 0; t < T; ++t)
         for (int32_t k = 0; k < K; ++k)
-            if (inv[t * K + k] >= num_rows)
+            if (inv[t * K + k] < -1 || inv[t * K + k] >= num_rows)
                 flags |= ORC_FLAG_INV_RANGE;
     for (int64_t t = 0; t < T; ++t) {
         for (int64_t h = 0; h < H; ++h) {

@@ -148,7 +148,7 @@ def pin_golden_unpermute(orc):
             w = np.array(case["topk_weights"], np.float32)
         inv = np.array(case["inv_permuted_idx"], np.int32)
         out, flags = orc.unpermute(rows, w, inv)
-        assert flags == 0
+        assert flags == case.get("flags", 0), case["name"]
         assert out.tolist() == case["out_bf16_bits"], case["name"]
         if "out" in case:
             assert bf16_bits_to_f64(out).tolist() == case["out"], case["name"]
@@ -341,6 +341,11 @@ def pin_flags(orc):
     rows = np.zeros((2, 3), np.uint16)
     _, f = orc.unpermute(rows, np.ones((1, 2), np.float32), np.array([0, 2], np.int32))
     assert f == 4
+    # below -1 names no row either; -1 itself is a dropped row, not an error
+    _, f = orc.unpermute(rows, np.ones((1, 2), np.float32), np.array([-2, 1], np.int32))
+    assert f == 4
+    _, f = orc.unpermute(rows, np.ones((1, 2), np.float32), np.array([-1, 1], np.int32))
+    assert f == 0
 
 
 # ------------------------------------------------------ fp8 quantisation ---

@@ -191,19 +191,24 @@ def test_fp8_scales_odd_width(T):
     check_case(inp)
 
 
-def test_unpermute_flags_bad_inverse_indices():
+@pytest.mark.parametrize("bad", [{5: "end"}, {11: -4}, {5: "end", 11: -4}, {3: -1}],
+                         ids=["past_end", "below_minus_one", "both", "minus_one_only"])
+def test_unpermute_flags_bad_inverse_indices(bad):
+    """An inverse index outside [-1, num_rows) names no row: it is skipped and
+    raises MOE_FLAG_INV_OUT_OF_RANGE; -1 is a dropped row and raises nothing.
+    The status word must equal the oracle's flags on the raw map."""
     T, K, H = 20, 3, 48
     rows = torch.randn(T * K, H).to(torch.bfloat16)
     w = torch.rand(T, K)
     inv = torch.randperm(T * K).to(torch.int32)
-    inv[5] = T * K       # past the end of rows
-    inv[11] = -4         # negative but not -1
+    for i, v in bad.items():
+        inv[i] = T * K if v == "end" else v
     ws = torch.empty(mp.moe_permute_workspace_size(T, K, 4), dtype=torch.uint8, device="cuda")
     mp.moe_permute_workspace_init(ws)
     out = gpu_unpermute(rows, w, inv, ws=ws)
-    assert mp.moe_read_status(ws) == mp.MOE_FLAG_INV_OUT_OF_RANGE
-    ref_out, flags = oracle.unpermute(bits16(rows), w.numpy(), np.where(inv.numpy() < -1, -1, inv.numpy()))
-    assert flags == oracle.FLAG_INV_RANGE
+    ref_out, flags = oracle.unpermute(bits16(rows), w.numpy(), inv.numpy())
+    assert mp.moe_read_status(ws) == flags
+    assert flags == (0 if bad == {3: -1} else oracle.FLAG_INV_RANGE)
     assert_unpermute_matches(bits16(out), ref_out)
     mp.moe_clear_status(ws)
     assert mp.moe_read_status(ws) == 0

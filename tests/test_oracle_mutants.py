@@ -47,6 +47,8 @@ MUTANTS = {
     "batched_slot_stride": ("int64_t slot = (int64_t)e * M + j;", "int64_t slot = (int64_t)e * (M - 1) + j;"),
     "batched_count_unclamped": ("expert_num_tokens[e] = (int32_t)(next[e] < M ? next[e] : M);",
                                 "expert_num_tokens[e] = (int32_t)next[e];"),
+    "inv_below_minus_one_not_flagged": ("if (inv[t * K + k] < -1 || inv[t * K + k] >= num_rows)",
+                                        "if (inv[t * K + k] >= num_rows)"),
     "quant_zero_group_scale": ("float scale = amax > 0.0f ? amax / 448.0f : 1.0f;",
                                "float scale = amax > 0.0f ? amax / 448.0f : 0.0f;"),
 }
