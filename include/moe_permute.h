@@ -21,7 +21,8 @@
  *  - Every pointer except the ones noted as host pointers is a DEVICE pointer
  *    to caller-owned, contiguous, row-major memory on the current device.
  *    The library never allocates, frees or synchronises (except
- *    moe_read_status, which synchronises the given stream by design); all
+ *    moe_read_status, which synchronises the given stream by design;
+ *    moe_permute_read_status is its asynchronous form); all
  *    device work is enqueued on `stream` in stream order, so the calls can be
  *    captured into a CUDA graph.
  *  - Return value: MOE_OK (0) or a negative moe_status_t.  Argument errors are
@@ -80,8 +81,11 @@ typedef enum { MOE_INDEX_INT32 = 0, MOE_INDEX_INT64 = 1 } moe_index_t;
 #define MOE_FLAG_MAP_OUT_OF_RANGE 2u  /* expert_map value not -1 and outside [0, num_local_experts) */
 #define MOE_FLAG_INV_OUT_OF_RANGE 4u  /* unpermute: inv index >= num_rows or < -1 */
 #define MOE_FLAG_BARRIER_TIMEOUT  8u  /* permute: a bounded wait for another block's
-                                         histogram gave up (outputs of that call are
-                                         undefined; re-initialise the workspace) */
+                                         histogram gave up.  The outputs of that call
+                                         are undefined; the workspace needs no
+                                         re-initialisation: every call tags its
+                                         histogram entries afresh, so the next call on
+                                         the same workspace is exact again */
 #define MOE_FLAG_CAPACITY_OVERFLOW 16u /* batched permute: an expert got more rows than
                                           its capacity; the extra rows were dropped */
 
@@ -266,6 +270,22 @@ MOE_API int moe_unpermute(const void *permuted_rows, int64_t num_rows,
 MOE_API int moe_read_status(const void *workspace, uint32_t *host_status,
                     moe_stream_t stream);
 
+/*
+ * moe_permute_read_status: the asynchronous form of moe_read_status.  Enqueues
+ * on `stream` one tiny kernel that copies the status word to `dst` and, when
+ * clear_after_read is non-zero, zeroes the word in the same step; nothing
+ * synchronises, so the call captures into a CUDA graph with the permutes it
+ * follows, and a serving loop reads each step's flags without a host round
+ * trip.  (vLLM PR #43014 digest, "review highlights": results go into the
+ * caller's buffers.)
+ *  dst  4-byte aligned memory the device can write: device or managed memory,
+ *       or page-locked host memory (cudaHostAlloc / cudaHostRegister).
+ *       Pageable host memory is refused with MOE_ERR_INVALID_ARG.  The value
+ *       is there once the stream has reached this call.
+ */
+MOE_API int moe_permute_read_status(void *workspace, uint32_t *dst, int clear_after_read,
+                                    moe_stream_t stream);
+
 /* moe_clear_status: zero the status word (async on `stream`). */
 MOE_API int moe_clear_status(void *workspace, moe_stream_t stream);
 
@@ -289,13 +309,17 @@ MOE_API int moe_clear_status(void *workspace, moe_stream_t stream);
  *  - Every call on a device shares the one array, which keeps the last call's
  *    contents.  Calls that may overlap on the GPU (two streams, or parallel
  *    graph branches) race on it; serialise them.
- *  - A call whose scratch need, moe_permute_workspace_size(num_tokens, topk,
- *    num_experts), exceeds MOE_NOALLOC_SCRATCH_BYTES returns
- *    MOE_ERR_WORKSPACE_TOO_SMALL and enqueues nothing: up to 256 experts fit
- *    for any token count, 512 experts up to 512 tokens, 1024 up to 256.
+ *  - Arguments are checked first, exactly as moe_permute checks them, and
+ *    before any device is touched.  Then a call whose scratch need,
+ *    moe_permute_workspace_size(num_tokens, topk, num_experts), exceeds
+ *    MOE_NOALLOC_SCRATCH_BYTES returns MOE_ERR_WORKSPACE_TOO_SMALL and
+ *    enqueues nothing: up to 256 experts fit for any token count, 512
+ *    experts up to 512 tokens, 1024 up to 256.  num_tokens = 0 always fits.
  *  - Device status flags (MOE_FLAG_*) are kept in the shared array and are
  *    not readable through this entry point; rows with bad ids are still
- *    dropped exactly as moe_permute drops them.
+ *    dropped exactly as moe_permute drops them.  After a bounded wait gave
+ *    up (MOE_FLAG_BARRIER_TIMEOUT in moe_permute's terms) the next call is
+ *    exact again with no re-initialisation, as for moe_permute.
  */
 #define MOE_NOALLOC_SCRATCH_BYTES ((size_t)(1u << 20) + 256u)
 MOE_API int moe_permute_noalloc(const void *hidden_states, moe_dtype_t hidden_dtype,

@@ -223,15 +223,36 @@ def moe_clear_status(workspace, stream=None) -> None:
     _b.check("moe_clear_status", _b.lib().moe_clear_status(_ptr(workspace), _stream(stream)))
 
 
+def moe_permute_read_status(workspace, dst, *, clear_after_read=False, stream=None) -> None:
+    """Enqueue a copy of the status word into dst (a 1-element int32/uint32
+    tensor on the device, or in pinned host memory) and optionally clear the
+    word; asynchronous and capturable into a CUDA graph."""
+    if dst.dtype.is_floating_point or dst.element_size() != 4 or dst.numel() < 1:
+        raise ValueError("dst must hold at least one 32-bit integer")
+    if not dst.is_contiguous():
+        raise ValueError("expected a contiguous tensor (the library writes in place)")
+    if not dst.is_cuda and not dst.is_pinned():
+        raise ValueError("dst must be device memory or pinned host memory")
+    _b.check("moe_permute_read_status", _b.lib().moe_permute_read_status(
+        _ptr(workspace), dst.data_ptr(), 1 if clear_after_read else 0, _stream(stream)))
+
+
 @dataclass
 class MoEPermuteScratch:
     """Buffers for repeated permutes, allocated once (vLLM PR #43014 digest,
-    "key source excerpts": MoEPermuteScratch.__post_init__ / validate).
+    "key source excerpts": MoEPermuteScratch.__post_init__, validate,
+    token_expert_indices_view, prepare_topk_ids).
 
     Holds the workspace and the metadata buffers for up to max_num_tokens
-    tokens, plus permuted hidden (and fp8 scale) rows when hidden_size is given.
-    ``permute`` validates its inputs against these sizes and writes into views
-    of the same storage on every call.
+    tokens, plus permuted hidden (and fp8 scale) rows when hidden_size is
+    given, the unpermute output [max_num_tokens, hidden_size] bf16, and, when
+    max_rows_per_expert is given, the batched layout's buffers.  Every method
+    validates its inputs against these sizes and writes into views of the same
+    storage on every call: nothing is allocated after construction.
+
+    The digest's sort workspace, sorted-row and int32-cast buffers have no
+    counterpart: the routing is a counting sort whose whole scratch is the
+    library's workspace, and int64 ids are read natively.
     """
     max_num_tokens: int
     topk: int
@@ -241,19 +262,31 @@ class MoEPermuteScratch:
     hidden_size: int | None = None
     hidden_dtype: torch.dtype | None = None
     scale_cols: int = 0
+    max_rows_per_expert: int | None = None
+    token_expert_indices: torch.Tensor = field(init=False)
     workspace: torch.Tensor = field(init=False)
     expert_first_token_offset: torch.Tensor = field(init=False)
     permuted_idx: torch.Tensor = field(init=False)
     inv_permuted_idx: torch.Tensor = field(init=False)
     permuted_hidden_states: torch.Tensor | None = field(init=False, default=None)
     permuted_scales: torch.Tensor | None = field(init=False, default=None)
+    unpermuted: torch.Tensor | None = field(init=False, default=None)
+    expert_num_tokens: torch.Tensor | None = field(init=False, default=None)
+    batched_hidden_states: torch.Tensor | None = field(init=False, default=None)
+    batched_scales: torch.Tensor | None = field(init=False, default=None)
 
     def __post_init__(self):
         dev = torch.device(self.device)
+        self.device = dev
         rows = self.max_num_tokens * self.topk
+        if not moe_permute_supported(dev.index if dev.index is not None else None):
+            raise MoeError("MoEPermuteScratch: the current device is not an sm_103 GPU")
         nbytes = moe_permute_workspace_size(self.max_num_tokens, self.topk, self.num_experts)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         moe_permute_workspace_init(self.workspace)
+        # r = t * topk + k; stored only so that token_expert_indices_view can
+        # hand out the digest's [T, topk] view (the kernels compute r).
+        self.token_expert_indices = torch.arange(rows, dtype=torch.int32, device=dev)
         self.expert_first_token_offset = torch.empty(self.num_local_experts + 1,
                                                      dtype=torch.int64, device=dev)
         self.permuted_idx = torch.empty(rows, dtype=torch.int32, device=dev)
@@ -264,14 +297,31 @@ class MoEPermuteScratch:
             if self.scale_cols:
                 self.permuted_scales = torch.empty(rows, self.scale_cols,
                                                    dtype=torch.float32, device=dev)
+            self.unpermuted = torch.empty(self.max_num_tokens, self.hidden_size,
+                                          dtype=torch.bfloat16, device=dev)
+        if self.max_rows_per_expert is not None:
+            slots = self.num_local_experts * int(self.max_rows_per_expert)
+            self.expert_num_tokens = torch.empty(self.num_local_experts, dtype=torch.int32,
+                                                 device=dev)
+            if self.hidden_size is not None:
+                self.batched_hidden_states = torch.empty(slots, self.hidden_size,
+                                                         dtype=self.hidden_dtype, device=dev)
+                if self.scale_cols:
+                    self.batched_scales = torch.empty(slots, self.scale_cols,
+                                                      dtype=torch.float32, device=dev)
 
     def validate(self, hidden_states, topk_ids, hidden_scales=None):
+        """Inputs must fit the sizes this scratch was built for."""
         n_token = topk_ids.shape[0]
+        if topk_ids.device != self.device:
+            raise ValueError("topk_ids is not on the scratch's device")
         if n_token > self.max_num_tokens:
             raise ValueError(f"{n_token} tokens > max_num_tokens={self.max_num_tokens}")
-        if topk_ids.shape[1] != self.topk:
+        if topk_ids.dim() != 2 or topk_ids.shape[1] != self.topk:
             raise ValueError("topk mismatch")
         if hidden_states is not None:
+            if hidden_states.device != self.device:
+                raise ValueError("hidden_states is not on the scratch's device")
             if hidden_states.shape[0] != n_token:
                 raise ValueError("hidden_states / topk_ids token count mismatch")
             if self.hidden_size is not None and (hidden_states.shape[1] != self.hidden_size
@@ -279,19 +329,38 @@ class MoEPermuteScratch:
                 raise ValueError("hidden size / dtype mismatch")
         if (hidden_scales is not None) != bool(self.scale_cols) and self.hidden_size is not None:
             raise ValueError("scales given iff the scratch holds scale rows")
+        if hidden_scales is not None and tuple(hidden_scales.shape) != (n_token, self.scale_cols):
+            raise ValueError(f"hidden_scales must be [{n_token}, {self.scale_cols}]")
+
+    def token_expert_indices_view(self, n_token: int) -> torch.Tensor:
+        """The expanded row ids r = t * topk + k of n_token tokens, as [n_token, topk]."""
+        if n_token > self.max_num_tokens:
+            raise ValueError(f"{n_token} tokens > max_num_tokens={self.max_num_tokens}")
+        return self.token_expert_indices[:n_token * self.topk].view(n_token, self.topk)
+
+    def prepare_topk_ids(self, topk_ids: torch.Tensor) -> torch.Tensor:
+        """The ids as the kernels take them: int32 and int64 are both read
+        natively, so this is the tensor itself (no cast, no copy)."""
+        if topk_ids.dtype not in _INDEX:
+            raise ValueError("topk_ids must be int32 or int64")
+        return topk_ids
+
+    def _rows(self, topk_ids):
+        return topk_ids.shape[0] * self.topk
 
     def permute(self, hidden_states, topk_ids, *, expert_map=None, hidden_scales=None,
                 stream=None):
         """Permute into this scratch; returns views sized for this call."""
         self.validate(hidden_states, topk_ids, hidden_scales)
-        n = topk_ids.shape[0] * self.topk
+        n = self._rows(topk_ids)
         ph = None
         ps = None
         if self.permuted_hidden_states is not None and hidden_states is not None:
             ph = self.permuted_hidden_states[:n]
             if hidden_scales is not None:
                 ps = self.permuted_scales[:n]
-        moe_permute(hidden_states, topk_ids, self.expert_first_token_offset,
+        moe_permute(hidden_states, self.prepare_topk_ids(topk_ids),
+                    self.expert_first_token_offset,
                     self.permuted_idx[:n], self.inv_permuted_idx[:n], self.workspace,
                     num_experts=self.num_experts, num_local_experts=self.num_local_experts,
                     expert_map=expert_map, hidden_scales=hidden_scales,
@@ -299,3 +368,77 @@ class MoEPermuteScratch:
         return dict(permuted_hidden_states=ph, permuted_scales=ps,
                     expert_first_token_offset=self.expert_first_token_offset,
                     permuted_idx=self.permuted_idx[:n], inv_permuted_idx=self.inv_permuted_idx[:n])
+
+    def permute_quant_fp8(self, hidden_states, topk_ids, *, expert_map=None, stream=None):
+        """Permute bf16 rows and quantise them to fp8 e4m3 on the way, into
+        this scratch's rows and scales.  The scratch must have been built with
+        hidden_dtype=torch.float8_e4m3fn and scale_cols = hidden_size / 128."""
+        if self.hidden_dtype != torch.float8_e4m3fn or self.hidden_size is None or \
+                self.scale_cols != self.hidden_size // _b.MOE_QUANT_GROUP:
+            raise ValueError("permute_quant_fp8 needs a scratch of float8_e4m3fn rows with "
+                             "hidden_size / 128 scale columns")
+        if hidden_states.dtype != torch.bfloat16 or hidden_states.device != self.device:
+            raise ValueError("permute_quant_fp8 takes bf16 hidden_states on the scratch's device")
+        if hidden_states.shape != (topk_ids.shape[0], self.hidden_size):
+            raise ValueError(f"hidden_states must be [{topk_ids.shape[0]}, {self.hidden_size}]")
+        self.validate(None, topk_ids)
+        n = self._rows(topk_ids)
+        codes = self.permuted_hidden_states[:n]
+        scales = self.permuted_scales[:n]
+        moe_permute_quant_fp8(hidden_states, self.prepare_topk_ids(topk_ids),
+                              self.expert_first_token_offset, self.permuted_idx[:n],
+                              self.inv_permuted_idx[:n], self.workspace, codes, scales,
+                              num_experts=self.num_experts,
+                              num_local_experts=self.num_local_experts, expert_map=expert_map,
+                              stream=stream)
+        return dict(permuted_hidden_states=codes, permuted_scales=scales,
+                    expert_first_token_offset=self.expert_first_token_offset,
+                    permuted_idx=self.permuted_idx[:n], inv_permuted_idx=self.inv_permuted_idx[:n])
+
+    def permute_batched(self, hidden_states, topk_ids, *, expert_map=None, hidden_scales=None,
+                        stream=None):
+        """Permute into this scratch's batched [E_local, M, H] layout
+        (M = max_rows_per_expert); inv_permuted_idx then holds slots e*M + j."""
+        if self.max_rows_per_expert is None:
+            raise ValueError("permute_batched needs a scratch built with max_rows_per_expert")
+        self.validate(hidden_states, topk_ids, hidden_scales)
+        n = self._rows(topk_ids)
+        bh = self.batched_hidden_states if hidden_states is not None else None
+        bs = self.batched_scales if hidden_states is not None else None
+        moe_permute_batched(hidden_states, self.prepare_topk_ids(topk_ids),
+                            self.expert_num_tokens, self.inv_permuted_idx[:n], self.workspace,
+                            num_experts=self.num_experts,
+                            max_rows_per_expert=self.max_rows_per_expert,
+                            num_local_experts=self.num_local_experts, expert_map=expert_map,
+                            hidden_scales=hidden_scales, batched_hidden_states=bh,
+                            batched_scales=bs, stream=stream)
+        M = int(self.max_rows_per_expert)
+        return dict(batched_hidden_states=None if bh is None
+                    else bh.view(self.num_local_experts, M, self.hidden_size),
+                    batched_scales=None if bs is None
+                    else bs.view(self.num_local_experts, M, self.scale_cols),
+                    expert_num_tokens=self.expert_num_tokens,
+                    inv_permuted_idx=self.inv_permuted_idx[:n])
+
+    def unpermute(self, permuted_rows, topk_weights, *, out=None, stream=None):
+        """Reduce the grouped GEMM's output rows back to tokens through the
+        inverse map the last permute of this scratch wrote (contiguous or
+        batched).  Writes into `out` if given, else into this scratch's
+        unpermute buffer; returns the [T, H] result."""
+        T = topk_weights.shape[0]
+        if T > self.max_num_tokens or topk_weights.dim() != 2 or topk_weights.shape[1] != self.topk:
+            raise ValueError("topk_weights must be [T, topk] with T <= max_num_tokens")
+        if out is None:
+            if self.unpermuted is None or permuted_rows.shape[1] != self.hidden_size:
+                raise ValueError("no unpermute buffer of this hidden size: pass out=")
+            out = self.unpermuted[:T]
+        moe_unpermute(permuted_rows, topk_weights, self.inv_permuted_idx[:T * self.topk], out,
+                      workspace=self.workspace, stream=stream)
+        return out
+
+    def read_status(self, stream=None) -> int:
+        """OR of the MOE_FLAG_* bits raised since the last clear (syncs the stream)."""
+        return moe_read_status(self.workspace, stream)
+
+    def clear_status(self, stream=None) -> None:
+        moe_clear_status(self.workspace, stream)

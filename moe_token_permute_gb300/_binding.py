@@ -54,6 +54,7 @@ SIGNATURES = {
     "moe_unpermute": (ctypes.c_int, [_P, _I64, _P, _P, _I64, _I64, _I32, _P, _P, _P]),
     "moe_read_status": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32), _P]),
     "moe_clear_status": (ctypes.c_int, [_P, _P]),
+    "moe_permute_read_status": (ctypes.c_int, [_P, _P, ctypes.c_int, _P]),
     "moe_permute_batched": (ctypes.c_int, [_P, ctypes.c_int, _P, _I64, _P, ctypes.c_int, _P,
                                            _I64, _I64, _I32, _I32, _I32, _I64,
                                            _P, _P, _P, _P, _P, _SZ, _P]),

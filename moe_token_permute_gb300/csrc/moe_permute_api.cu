@@ -458,6 +458,67 @@ int elem_bytes(moe_dtype_t dt) {
   }
 }
 
+// Host checks of moe_permute's arguments, before anything touches a device.
+// check_workspace_ptr: false when the caller supplies the scratch itself
+// (moe_permute_noalloc); workspace_bytes is then the scratch's size.
+int permute_args_status(const void* hidden_states, moe_dtype_t hidden_dtype,
+                        const float* hidden_scales, int64_t scale_cols, const void* topk_ids,
+                        moe_index_t topk_ids_dtype, const int32_t* expert_map, int64_t T,
+                        int64_t H, int32_t topk, int32_t num_experts, int32_t num_local_experts,
+                        const void* permuted_hidden_states, const float* permuted_scales,
+                        const int64_t* expert_first_token_offset, const int32_t* permuted_idx,
+                        const int32_t* inv_permuted_idx, bool check_workspace_ptr,
+                        const void* workspace, size_t workspace_bytes) {
+  const int eb = elem_bytes(hidden_dtype);
+  if (eb == 0 || T < 0 || H < 1 || topk < 1 || topk > MOE_MAX_TOPK || num_experts < 1 ||
+      num_local_experts < 1 || num_local_experts > num_experts ||
+      num_local_experts > MOE_MAX_LOCAL_EXPERTS)
+    return MOE_ERR_INVALID_ARG;
+  if (expert_map == nullptr && num_local_experts != num_experts) return MOE_ERR_INVALID_ARG;
+  if (topk_ids_dtype != MOE_INDEX_INT32 && topk_ids_dtype != MOE_INDEX_INT64)
+    return MOE_ERR_INVALID_ARG;
+  if (T > INT32_MAX / topk) return MOE_ERR_INVALID_ARG;
+  if (H > INT64_MAX / 16 / eb) return MOE_ERR_INVALID_ARG;
+  if (expert_first_token_offset == nullptr || !aligned(expert_first_token_offset, 8))
+    return MOE_ERR_INVALID_ARG;
+  if (scale_cols < 0) return MOE_ERR_INVALID_ARG;
+  // With T = 0 only the offsets are written; empty tensors may come as NULL.
+  if (T == 0) return MOE_OK;
+  const size_t id_bytes = topk_ids_dtype == MOE_INDEX_INT64 ? 8 : 4;
+  if (topk_ids == nullptr || !aligned(topk_ids, id_bytes)) return MOE_ERR_INVALID_ARG;
+  if (expert_map != nullptr && !aligned(expert_map, 4)) return MOE_ERR_INVALID_ARG;
+  if (permuted_idx == nullptr || inv_permuted_idx == nullptr || !aligned(permuted_idx, 4) ||
+      !aligned(inv_permuted_idx, 4))
+    return MOE_ERR_INVALID_ARG;
+  if (permuted_hidden_states != nullptr && hidden_states == nullptr) return MOE_ERR_INVALID_ARG;
+  const bool with_scales = hidden_scales != nullptr || permuted_scales != nullptr;
+  if (with_scales) {
+    if (hidden_scales == nullptr || permuted_scales == nullptr || scale_cols < 1 ||
+        permuted_hidden_states == nullptr || !aligned(hidden_scales, 4) ||
+        !aligned(permuted_scales, 4))
+      return MOE_ERR_INVALID_ARG;
+  } else if (scale_cols != 0) {
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (check_workspace_ptr && (workspace == nullptr || !aligned(workspace, 256)))
+    return MOE_ERR_INVALID_ARG;
+  if (workspace_bytes < workspace_bytes_for(T, topk, num_experts))
+    return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return MOE_OK;
+}
+
+// Copy of the status word for moe_permute_read_status: one thread, so that
+// the destination may be device memory or pinned host memory, and the read
+// (and the optional clear) stay ordered in the stream like any kernel.
+__global__ void k_copy_status(unsigned* __restrict__ status, uint32_t* __restrict__ dst,
+                              int clear) {
+  pdl_wait();
+  if (threadIdx.x == 0) {
+    *dst = *status;
+    if (clear) *status = 0u;
+  }
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -509,45 +570,18 @@ int moe_permute(const void* hidden_states, moe_dtype_t hidden_dtype, const float
                 float* permuted_scales, int64_t* expert_first_token_offset, int32_t* permuted_idx,
                 int32_t* inv_permuted_idx, void* workspace, size_t workspace_bytes,
                 moe_stream_t stream) {
-  const int eb = elem_bytes(hidden_dtype);
-  const int64_t T = num_tokens, H = hidden_size;
-  if (eb == 0 || T < 0 || H < 1 || topk < 1 || topk > MOE_MAX_TOPK || num_experts < 1 ||
-      num_local_experts < 1 || num_local_experts > num_experts ||
-      num_local_experts > MOE_MAX_LOCAL_EXPERTS)
-    return MOE_ERR_INVALID_ARG;
-  if (expert_map == nullptr && num_local_experts != num_experts) return MOE_ERR_INVALID_ARG;
-  if (topk_ids_dtype != MOE_INDEX_INT32 && topk_ids_dtype != MOE_INDEX_INT64)
-    return MOE_ERR_INVALID_ARG;
-  if (T > INT32_MAX / topk) return MOE_ERR_INVALID_ARG;
-  if (H > INT64_MAX / 16 / eb) return MOE_ERR_INVALID_ARG;
-  if (expert_first_token_offset == nullptr || !aligned(expert_first_token_offset, 8))
-    return MOE_ERR_INVALID_ARG;
-  if (scale_cols < 0) return MOE_ERR_INVALID_ARG;
-  // With T = 0 only the offsets are written; empty tensors may come as NULL.
-  if (T > 0) {
-    const size_t id_bytes = topk_ids_dtype == MOE_INDEX_INT64 ? 8 : 4;
-    if (topk_ids == nullptr || !aligned(topk_ids, id_bytes)) return MOE_ERR_INVALID_ARG;
-    if (expert_map != nullptr && !aligned(expert_map, 4)) return MOE_ERR_INVALID_ARG;
-    if (permuted_idx == nullptr || inv_permuted_idx == nullptr || !aligned(permuted_idx, 4) ||
-        !aligned(inv_permuted_idx, 4))
-      return MOE_ERR_INVALID_ARG;
-    if (permuted_hidden_states != nullptr && hidden_states == nullptr) return MOE_ERR_INVALID_ARG;
-    const bool with_scales = hidden_scales != nullptr || permuted_scales != nullptr;
-    if (with_scales) {
-      if (hidden_scales == nullptr || permuted_scales == nullptr || scale_cols < 1 ||
-          permuted_hidden_states == nullptr || !aligned(hidden_scales, 4) ||
-          !aligned(permuted_scales, 4))
-        return MOE_ERR_INVALID_ARG;
-    } else if (scale_cols != 0) {
-      return MOE_ERR_INVALID_ARG;
-    }
-    if (workspace == nullptr || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
-    if (workspace_bytes < workspace_bytes_for(T, topk, num_experts))
-      return MOE_ERR_WORKSPACE_TOO_SMALL;
-  }
+  const int rc = permute_args_status(hidden_states, hidden_dtype, hidden_scales, scale_cols,
+                                     topk_ids, topk_ids_dtype, expert_map, num_tokens,
+                                     hidden_size, topk, num_experts, num_local_experts,
+                                     permuted_hidden_states, permuted_scales,
+                                     expert_first_token_offset, permuted_idx, inv_permuted_idx,
+                                     /*check_workspace_ptr=*/true, workspace, workspace_bytes);
+  if (rc != MOE_OK) return rc;
   const DeviceInfo* d = current_device();
   if (!is_supported(d)) return MOE_ERR_UNSUPPORTED_DEVICE;
 
+  const int64_t T = num_tokens, H = hidden_size;
+  const int eb = elem_bytes(hidden_dtype);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t err;
   if (T == 0) {
@@ -730,6 +764,25 @@ int moe_clear_status(void* workspace, moe_stream_t stream) {
   return MOE_OK;
 }
 
+int moe_permute_read_status(void* workspace, uint32_t* dst, int clear_after_read,
+                            moe_stream_t stream) {
+  if (workspace == nullptr || dst == nullptr || !aligned(workspace, 256) || !aligned(dst, 4))
+    return MOE_ERR_INVALID_ARG;
+  // The kernel writes through dst, so it must be memory the device can
+  // reach: device (or managed) memory, or page-locked host memory.
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, dst) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (a.type == cudaMemoryTypeUnregistered) return MOE_ERR_INVALID_ARG;
+  if (!is_supported(current_device())) return MOE_ERR_UNSUPPORTED_DEVICE;
+  unsigned* status = &static_cast<WsHeader*>(workspace)->status;
+  const cudaError_t err = launch(k_copy_status, 1, 32, 0, reinterpret_cast<cudaStream_t>(stream),
+                                 status, dst, clear_after_read != 0 ? 1 : 0);
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 }  // extern "C"
 
 // ---- allocation-free variant of moe_permute ------------------------------
@@ -753,12 +806,22 @@ extern "C" int moe_permute_noalloc(const void* hidden_states, moe_dtype_t hidden
                                    float* permuted_scales, int64_t* expert_first_token_offset,
                                    int32_t* permuted_idx, int32_t* inv_permuted_idx,
                                    moe_stream_t stream) {
-  if (num_tokens >= 0 && topk >= 1 && topk <= MOE_MAX_TOPK && num_experts >= 1 &&
-      num_tokens <= INT32_MAX / topk &&
-      workspace_bytes_for(num_tokens, topk, num_experts) > MOE_NOALLOC_SCRATCH_BYTES)
-    return MOE_ERR_WORKSPACE_TOO_SMALL;
+  // moe_permute's own argument checks first, with the static array standing
+  // in for the workspace: a request it cannot hold is
+  // MOE_ERR_WORKSPACE_TOO_SMALL, decided before any device is touched.
+  const int rc = permute_args_status(hidden_states, hidden_dtype, hidden_scales, scale_cols,
+                                     topk_ids, topk_ids_dtype, expert_map, num_tokens,
+                                     hidden_size, topk, num_experts, num_local_experts,
+                                     permuted_hidden_states, permuted_scales,
+                                     expert_first_token_offset, permuted_idx, inv_permuted_idx,
+                                     /*check_workspace_ptr=*/false, nullptr,
+                                     MOE_NOALLOC_SCRATCH_BYTES);
+  if (rc != MOE_OK) return rc;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
@@ -769,9 +832,11 @@ extern "C" int moe_permute_noalloc(const void* hidden_states, moe_dtype_t hidden
         cudaGetLastError();
         return MOE_ERR_CUDA;
       }
-      if (cudaMemsetAsync(ptr, 0, MOE_NOALLOC_SCRATCH_BYTES, reinterpret_cast<cudaStream_t>(stream)) !=
-          cudaSuccess)
+      if (cudaMemsetAsync(ptr, 0, MOE_NOALLOC_SCRATCH_BYTES,
+                          reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
         return MOE_ERR_CUDA;
+      }
       g_noalloc_ptr[dev] = ptr;
     }
     scratch = g_noalloc_ptr[dev];

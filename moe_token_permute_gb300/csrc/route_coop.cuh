@@ -34,7 +34,8 @@
 // Every wait for a table entry is bounded (2^24 polls or 2 s): on timeout the
 // status word gets MOE_FLAG_BARRIER_TIMEOUT and the kernel returns (outputs
 // undefined; the gather that follows never stores through an out-of-range
-// position; re-initialise the workspace before its next use).
+// position).  Block 0 still advances gen on that path, so the next call tags
+// its entries afresh and is exact without re-initialising the workspace.
 #pragma once
 
 #include "common.cuh"

@@ -80,11 +80,26 @@ def assert_metadata_equal(bufs, ref):
     np.testing.assert_array_equal(bufs["inv"].cpu().numpy(), ref["inv_permuted_idx"])
 
 
+def assert_bytes_equal(got: np.ndarray, ref: np.ndarray, what: str, chunk_rows: int = 1 << 16):
+    """Row-by-row byte equality of two [rows, row_bytes] arrays, compared in
+    chunks so that gigabyte outputs need no gigabyte temporaries."""
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    for r0 in range(0, got.shape[0], chunk_rows):
+        g, f = got[r0:r0 + chunk_rows], ref[r0:r0 + chunk_rows]
+        if not np.array_equal(g, f):
+            bad = np.flatnonzero((g != f).reshape(g.shape[0], -1).any(axis=1))
+            raise AssertionError(f"{what}: {bad.size} rows differ from row {r0 + int(bad[0])} on")
+
+
 def assert_rows_equal_full(inp, bufs, ref_full):
+    """Every kept permuted row (p < N_valid) and scale row, bit for bit."""
     n = ref_full["n_valid"]
-    np.testing.assert_array_equal(bytes_of(bufs["ph"][:n]), ref_full["permuted_hidden"][:n])
+    assert_bytes_equal(bytes_of(bufs["ph"][:n]), ref_full["permuted_hidden"][:n].reshape(n, -1),
+                       "permuted_hidden_states")
     if bufs["ps"] is not None:
-        np.testing.assert_array_equal(bufs["ps"][:n].cpu().numpy(), ref_full["permuted_scales"][:n])
+        assert_bytes_equal(bytes_of(bufs["ps"][:n]),
+                           np.ascontiguousarray(ref_full["permuted_scales"][:n]).view(np.uint8).reshape(n, -1),
+                           "permuted_scales")
 
 
 def oracle_full(inp):
@@ -106,12 +121,18 @@ def gpu_unpermute(rows, weights, inv, ws=None, device=DEV):
 
 
 def assert_unpermute_matches(got_bits: np.ndarray, ref_bits: np.ndarray):
-    got = pins.bf16_bits_to_f64(got_bits)
-    ref = pins.bf16_bits_to_f64(ref_bits)
+    """Every element within 2^-7*|ref| + 1e-6 of the oracle, and in fact equal
+    bit for bit: both sides take the same fp32 operations in the same order.
+    Elements equal in their bits pass both; the tolerance is evaluated on the
+    others, so that the check stays cheap on gigabyte outputs."""
+    assert got_bits.shape == ref_bits.shape
+    diff = got_bits != ref_bits
+    mism = int(np.count_nonzero(diff))
+    if mism == 0:
+        return
+    got = pins.bf16_bits_to_f64(got_bits[diff])
+    ref = pins.bf16_bits_to_f64(ref_bits[diff])
     err = np.abs(got - ref)
     bound = UNPERMUTE_RTOL * np.abs(ref) + UNPERMUTE_ATOL
     assert np.all(err <= bound), f"max excess {float((err - bound).max())}"
-    # Both sides take the same fp32 operations in the same order, so the
-    # results are expected to be identical bit for bit.
-    mism = int((got_bits != ref_bits).sum())
-    assert mism == 0, f"{mism} elements differ in their bits (within tolerance)"
+    raise AssertionError(f"{mism} elements differ in their bits (within tolerance)")

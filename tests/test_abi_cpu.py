@@ -138,6 +138,11 @@ def test_status_calls_reject_bad_workspace(lib):
     assert lib.moe_read_status(None, ctypes.byref(v), None) == b.MOE_ERR_INVALID_ARG
     assert lib.moe_clear_status(0x10010, None) == b.MOE_ERR_INVALID_ARG
     assert lib.moe_permute_workspace_init(0x10000, 16, None) == b.MOE_ERR_INVALID_ARG
+    # the asynchronous read: NULL or misaligned workspace, NULL or misaligned dst
+    assert lib.moe_permute_read_status(None, 0x2000, 0, None) == b.MOE_ERR_INVALID_ARG
+    assert lib.moe_permute_read_status(0x10010, 0x2000, 0, None) == b.MOE_ERR_INVALID_ARG
+    assert lib.moe_permute_read_status(0x10000, None, 1, None) == b.MOE_ERR_INVALID_ARG
+    assert lib.moe_permute_read_status(0x10000, 0x2002, 1, None) == b.MOE_ERR_INVALID_ARG
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
@@ -212,3 +217,28 @@ def test_noalloc_rejects_problems_beyond_its_scratch_on_host(lib):
                      out=0x3000, out_scales=None, offsets=0x4000, pidx=0x5000, inv=0x6000,
                      stream=None).values())
     assert lib.moe_permute_noalloc(*args) == b.MOE_ERR_WORKSPACE_TOO_SMALL
+
+
+def _noalloc_args(**over):
+    args = dict(hidden=0x1000, dt=b.MOE_DTYPE_BF16, scales=None, scale_cols=0, ids=0x2000,
+                idt=b.MOE_INDEX_INT32, emap=None, T=4096, H=8, K=2, E=512, EL=512,
+                out=0x3000, out_scales=None, offsets=0x4000, pidx=0x5000, inv=0x6000,
+                stream=None)
+    args.update(over)
+    return list(args.values())
+
+
+@pytest.mark.parametrize("over", [dict(K=0), dict(ids=None), dict(EL=5), dict(offsets=0x4004),
+                                  dict(dt=9), dict(scale_cols=3)])
+def test_noalloc_checks_arguments_before_its_scratch_size(lib, over):
+    # invalid arguments are reported as such, even for a problem the static
+    # scratch could not hold
+    assert lib.moe_permute_noalloc(*_noalloc_args(**over)) == b.MOE_ERR_INVALID_ARG
+
+
+def test_noalloc_empty_batch_fits_whatever_the_expert_count(lib):
+    # T = 0 needs no table: not MOE_ERR_WORKSPACE_TOO_SMALL even with 1024 experts
+    # (without a GPU the call then stops at the device lookup)
+    rc = lib.moe_permute_noalloc(*_noalloc_args(T=0, E=1024, EL=1024, hidden=None, out=None,
+                                                ids=None, pidx=None, inv=None))
+    assert rc in (b.MOE_OK, b.MOE_ERR_CUDA)

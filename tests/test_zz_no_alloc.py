@@ -2,14 +2,18 @@
 allocate device memory (for example a plugin whose host framework owns every
 allocation, or a serving loop that must not call cudaMalloc once running).
 It keeps its scratch in a static device array inside the library instead of
-a caller workspace.  This test calls it through the C ABI twice in a row, on
-different batches, and checks each result against moe_permute with a caller
-workspace: indices, offsets and rows must be identical (the bar for integer
-and byte outputs).  It is collected last and needs nothing from other tests."""
+a caller workspace.  This test calls it through the C ABI several times in a
+row, on different batches that share that array, and checks each result
+against the CPU oracle (indices, offsets, every kept row and scale row, bit
+for bit) and against moe_permute with a caller workspace.  It is collected
+last and needs nothing from other tests."""
+import numpy as np
 import pytest
 import torch
 
 import moe_token_permute_gb300 as mp
+import oracle
+from gpu_util import assert_bytes_equal, bytes_of
 from moe_token_permute_gb300 import _binding as b
 from moe_token_permute_gb300 import build as cuda_build
 from moe_token_permute_gb300.workloads import make_inputs
@@ -75,6 +79,32 @@ def test_noalloc_matches_workspace_entry_point_two_calls_in_a_row():
         assert torch.equal(got["ph"][:n].view(torch.uint8), ref["ph"][:n].view(torch.uint8))
         if sc_cols:
             assert torch.equal(got["ps"][:n], ref["ps"][:n])
+        # and against the oracle itself
+        orc = oracle.permute(inp["topk_ids"].cpu().numpy(), wl.E,
+                             expert_map=None if inp["expert_map"] is None
+                             else inp["expert_map"].cpu().numpy(),
+                             E_local=wl.e_local, hidden=bytes_of(inp["hidden"]),
+                             scales=None if inp["scales"] is None else inp["scales"].cpu().numpy())
+        assert orc["flags"] == 0 and orc["n_valid"] == n
+        np.testing.assert_array_equal(got["off"].cpu().numpy(), orc["offsets"])
+        np.testing.assert_array_equal(got["pidx"].cpu().numpy(), orc["permuted_idx"])
+        np.testing.assert_array_equal(got["inv"].cpu().numpy(), orc["inv_permuted_idx"])
+        assert_bytes_equal(bytes_of(got["ph"][:n]), orc["permuted_hidden"][:n], name)
+        if sc_cols:
+            np.testing.assert_array_equal(got["ps"][:n].cpu().numpy().view(np.uint32),
+                                          orc["permuted_scales"][:n].view(np.uint32))
+
+
+def test_noalloc_empty_batch_with_many_experts():
+    """T = 0 needs no histogram table: the offsets are zeroed whatever the
+    expert count, and the call succeeds."""
+    E = 1024
+    off = torch.full((E + 1,), 9, dtype=torch.int64, device="cuda")
+    rc = b.lib().moe_permute_noalloc(None, b.MOE_DTYPE_BF16, None, 0, None, b.MOE_INDEX_INT32,
+                                     None, 0, 64, 8, E, E, None, None, off.data_ptr(), None, None,
+                                     torch.cuda.current_stream().cuda_stream)
+    assert rc == b.MOE_OK
+    assert torch.count_nonzero(off).item() == 0
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch():
