@@ -23,6 +23,7 @@ import hashlib
 import json
 import os
 import statistics
+import subprocess
 import sys
 import threading
 import time
@@ -444,6 +445,28 @@ def graph_us(fns, n=100):
     return 1e3 * a.elapsed_time(b) / (reps * n)
 
 
+def c_abi_latency(name, T, iters=300):
+    """Per-call latency through the C ABI from a plain C program (no Python in
+    the loop), medians in us: *_c_abi_issue_us = host time per call of
+    back-to-back calls; *_c_abi_sync_us = one call plus a stream synchronise,
+    after an idle gap; *_c_abi_device_us = CUDA events around one call after
+    an idle gap.  Empty if the probe cannot be built or run."""
+    from moe_token_permute_gb300 import build as cuda_build
+    wl = WORKLOADS[name]
+    fp8 = name == "dsv3"
+    args = [wl.H, wl.E, wl.e_local, wl.K, 2 if fp8 else 0, wl.H // 128 if fp8 else 0, T, iters]
+    try:
+        exe = cuda_build.build_c_latency()
+        outp = subprocess.run([exe] + [str(a) for a in args], capture_output=True, text=True,
+                              timeout=120, check=True).stdout
+        r = json.loads(outp.strip().splitlines()[-1])
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError) as exc:
+        print(f"c_abi_latency {name} T={T}: {exc}", file=sys.stderr)
+        return {}
+    return {f"{op}_c_abi_{kind}_us": r[f"{op}_{kind}_us"]
+            for op in ("permute", "unpermute") for kind in ("issue", "sync", "device")}
+
+
 def sweep(dev, peak, flush):
     """Per (workload, T): permute and unpermute timed separately, rotating over
     enough buffer sets that the footprint is at least 3x the L2 size (or 64
@@ -498,6 +521,7 @@ def sweep(dev, peak, flush):
             if T == 1:
                 rec["permute_after_flush_us"] = round(timed_calls(s0.permute, 50, flush), 2)
                 rec["unpermute_after_flush_us"] = round(timed_calls(s0.unpermute, 50, flush), 2)
+                rec.update(c_abi_latency(name, T))
             rows.append(rec)
             del sets, first, s0
             torch.cuda.empty_cache()

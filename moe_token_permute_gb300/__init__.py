@@ -277,6 +277,8 @@ class MoEPermuteScratch:
 
     def __post_init__(self):
         dev = torch.device(self.device)
+        if dev.type == "cuda" and dev.index is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
         self.device = dev
         rows = self.max_num_tokens * self.topk
         if not moe_permute_supported(dev.index if dev.index is not None else None):
@@ -327,7 +329,8 @@ class MoEPermuteScratch:
             if self.hidden_size is not None and (hidden_states.shape[1] != self.hidden_size
                                                  or hidden_states.dtype != self.hidden_dtype):
                 raise ValueError("hidden size / dtype mismatch")
-        if (hidden_scales is not None) != bool(self.scale_cols) and self.hidden_size is not None:
+        if hidden_states is not None and self.hidden_size is not None and \
+                (hidden_scales is not None) != bool(self.scale_cols):
             raise ValueError("scales given iff the scratch holds scale rows")
         if hidden_scales is not None and tuple(hidden_scales.shape) != (n_token, self.scale_cols):
             raise ValueError(f"hidden_scales must be [{n_token}, {self.scale_cols}]")

@@ -91,5 +91,29 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB_PATH
 
 
+C_LATENCY_SOURCE = os.path.join(PKG, "c_latency.c")
+C_LATENCY_PATH = os.path.join(OUT_DIR, "moe_c_latency")
+
+
+def build_c_latency() -> str:
+    """Compile the C latency probe (c_latency.c) against the library and the
+    CUDA runtime with the host C compiler; returns the executable's path."""
+    build()
+    exe = C_LATENCY_PATH
+    if os.path.exists(exe) and all(os.path.getmtime(f) <= os.path.getmtime(exe)
+                                   for f in (C_LATENCY_SOURCE, LIB_PATH)):
+        return exe
+    nvcc = _nvcc()
+    cuda_inc = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc))), "include")
+    cudart_dir = _cuda_lib_dir(nvcc)
+    tmp = exe + f".tmp{os.getpid()}"
+    subprocess.check_call(
+        ["gcc", "-std=c11", "-O2", "-Wall", "-Wextra", "-Werror", "-I", INCLUDE, "-I", cuda_inc,
+         C_LATENCY_SOURCE, "-L", OUT_DIR, "-lmoe_permute", "-L", cudart_dir, "-lcudart",
+         f"-Wl,-rpath,{OUT_DIR}:{cudart_dir}", "-o", tmp])
+    os.replace(tmp, exe)
+    return exe
+
+
 if __name__ == "__main__":
     print(build(force=True, verbose="--verbose" in sys.argv))

@@ -5,8 +5,8 @@
 // the grouped GEMM.  This kernel moves the rows with the Blackwell bulk-copy
 // engine instead of registers: lane 0 of each warp copies a row chunk (up to
 // kTmaChunkBytes) from HBM into a shared-memory stage with
-// cp.async.bulk (completion counted on an mbarrier), then writes it to each of
-// the token's K destinations with cp.async.bulk stores.  No registers hold
+// cp.async.bulk (completion counted on an mbarrier), then lanes 0..K-1 write
+// it to the token's K destinations with one cp.async.bulk store each.  No registers hold
 // data in flight, so shared memory bounds the bytes in flight (~190 KB per
 // SM) rather than the register file.
 //
@@ -177,31 +177,31 @@ k_gather_rows_tma(const char* __restrict__ hidden, int64_t row_bytes, int64_t ch
         int j = i;
         for (int64_t it = item; it < n_items && j < i + kTmaStages; it += n_gw, ++j)
           (void)mbar_wait_bounded(&bars[j % kTmaStages], static_cast<uint32_t>(j / kTmaStages) & 1u);
-        bulk_wait_all();
       }
+      bulk_wait_all();
       __syncwarp();
       return;
     }
-    unsigned m = valid;
-    while (m != 0u) {
-      const int k = __ffs(m) - 1;
-      m &= m - 1u;
-      const int pk = __shfl_sync(kFullMask, p, k);
-      if (lane == 0) bulk_store(out + static_cast<int64_t>(pk) * row_bytes + c0, stages + s * pitch, bytes);
+    // Lane k stores the chunk to destination k: one thread's bulk copies go
+    // out one after another, so K stores from one lane took K times as long
+    // to issue.
+    if ((valid >> lane) & 1u) {
+      bulk_store(out + static_cast<int64_t>(p) * row_bytes + c0, stages + s * pitch, bytes);
+      bulk_commit();
     }
-    if (lane == 0) bulk_commit();
     if (with_scales && valid != 0u)
       store_token_scales(scales + t * scale_cols, scale_cols, sc, out_scales, p, valid);
     // Refill this stage with the item kTmaStages steps ahead once the stores
-    // just issued have read it.
+    // just issued (by any lane) have read it.
     const int64_t next = item + kTmaStages * n_gw;
-    if (lane == 0 && next < n_items) {
+    if (next < n_items) {
       bulk_wait_read<0>();
-      issue_load(next, s);
+      __syncwarp();
+      if (lane == 0) issue_load(next, s);
     }
     __syncwarp();
   }
-  if (lane == 0) bulk_wait_all();
+  bulk_wait_all();
 }
 
 }  // namespace moe

@@ -10,6 +10,9 @@
 //   R = T*K <= kFusedMaxRows: one launch of k_permute_fused; every block
 //     redundantly ranks all rows and the blocks share the row copy (no
 //     inter-block communication);
+//   with an expert map and 16-byte aligned rows: k_permute_onepass, one
+//     cooperative launch that routes a block of tokens and copies the rows of
+//     the tokens that keep one;
 //   otherwise: k_route_coop (cooperative grid; its blocks exchange their
 //     histograms through a tagged table in the workspace) writes the
 //     metadata, and the row gather (k_gather_rows_tma or k_gather_rows),
@@ -38,6 +41,7 @@
 #include "route_coop.cuh"
 #include "quant.cuh"
 #include "gather_tma.cuh"
+#include "onepass.cuh"
 
 namespace moe {
 namespace {
@@ -349,6 +353,95 @@ cudaError_t launch_gather_any(size_t vb, const void* hidden, int64_t row_bytes,
   }
 }
 
+// Stages in the single-launch permute's ring, at most.
+constexpr int64_t kOpMaxStages = 1024;
+static_assert(kOpMaxStages % kOpRouteWarps == 0, "stages come in multiples of the consumer warps");
+
+// Geometry of the single-launch large-batch permute (k_permute_onepass).
+struct OnepassPlan {
+  bool ok = false;
+  int64_t blocks = 0, tpb = 0, chunk = 0, pitch = 0;
+  int J = 0, n_chunks = 0, n_stages = 0;
+  size_t smem = 0;
+};
+
+OnepassPlan onepass_plan(int64_t T, int K, int E, int E_local, bool with_map, int64_t row_bytes,
+                         const DeviceInfo* d) {
+  OnepassPlan p;
+  // One block per SM (or one per token when there are fewer tokens); each
+  // block's rows must fit one ranking round of its 512 routing threads.
+  int64_t B = std::min<int64_t>(d->sm_count, T);
+  p.tpb = ceil_div(T, B);
+  B = ceil_div(T, p.tpb);
+  const int64_t rows = p.tpb * K;
+  if (rows > static_cast<int64_t>(kOpRouteThreads) * 4) return p;
+  p.J = rows <= static_cast<int64_t>(kOpRouteThreads) * 2 ? 2 : 4;
+  p.blocks = B;
+  p.n_chunks = static_cast<int>(ceil_div(row_bytes, kOpChunkBytes));
+  p.chunk = ceil_div(ceil_div(row_bytes, p.n_chunks), 16) * 16;
+  p.n_chunks = static_cast<int>(ceil_div(row_bytes, p.chunk));
+  p.pitch = ceil_div(p.chunk, 128) * 128;
+  const int64_t ints = (E_local + 1) + 3 * static_cast<int64_t>(E_local) +
+                       static_cast<int64_t>(kOpRouteWarps) * E_local + rows + 2 * p.tpb +
+                       (with_map ? E : 0);
+  const int64_t int_bytes = ints * 4;
+  const int64_t static_bytes = 1024;  // the kernel's static shared memory, rounded up
+  const int64_t avail = static_cast<int64_t>(d->max_smem_optin) - int_bytes - static_bytes;
+  const int64_t per_stage = p.pitch + 2 * static_cast<int64_t>(sizeof(uint64_t)) + 4;
+  // A multiple of the 16 consumer warps (one consumer per stage), enough for
+  // the block's items or as many as fit.
+  const int64_t items = p.tpb * p.n_chunks;
+  int64_t n = std::min<int64_t>(avail / per_stage, std::max<int64_t>(16, ceil_div(items, 16) * 16));
+  n = std::min<int64_t>(n, kOpMaxStages) / kOpRouteWarps * kOpRouteWarps;
+  if (n < kOpRouteWarps) return p;
+  p.n_stages = static_cast<int>(n);
+  p.smem = static_cast<size_t>(n * per_stage + int_bytes);
+  p.ok = true;
+  return p;
+}
+
+template <typename IdT>
+cudaError_t launch_onepass(const OnepassPlan& g, const IdT* ids, const int32_t* emap, int64_t T,
+                           int K, int E, int E_local, const void* hidden, int64_t row_bytes,
+                           const float* scales, int64_t scale_cols, void* out, float* out_scales,
+                           int64_t num_out_rows, int64_t* offsets, int32_t* pidx, int32_t* inv,
+                           WsHeader* hdr, cudaStream_t s, int64_t M = 0,
+                           int32_t* expert_num_tokens = nullptr) {
+  auto kern = g.J == 2 ? k_permute_onepass<IdT, 2> : k_permute_onepass<IdT, 4>;
+  cudaError_t err = allow_smem(kern, g.smem);
+  if (err != cudaSuccess) return err;
+#ifdef MOE_DEBUG_HOOKS
+  if (g.blocks + g_debug_extra_rows_host > std::min(T, kCoopMaxBlocks)) return cudaErrorInvalidValue;
+#endif
+  unsigned* table = reinterpret_cast<unsigned*>(reinterpret_cast<char*>(hdr) + kWsHeaderBytes);
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(static_cast<unsigned>(g.blocks));
+  cfg.blockDim = dim3(kOpThreads);
+  cfg.dynamicSmemBytes = g.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;  // every block waits for the others' table rows
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, ids, emap, T, K, E, E_local,
+                            static_cast<const char*>(hidden), row_bytes, g.chunk, g.n_chunks,
+                            g.n_stages, g.pitch, scales, scale_cols, static_cast<char*>(out),
+                            out_scales, num_out_rows, offsets, pidx, inv, hdr, table, M,
+                            expert_num_tokens);
+}
+
+// Whether the single-launch large-batch permute serves this call: an expert
+// map (it reads only the tokens that keep a row, which pays when the map
+// drops most rows; without a map the two-kernel path measured faster),
+// 16-byte aligned rows (bulk copies) and a plan that fits.
+bool use_onepass(const int32_t* emap, size_t vb, const void* out, const OnepassPlan& g) {
+  return emap != nullptr && out != nullptr && vb == 16 && g.ok;
+}
+
 template <typename IdT>
 cudaError_t permute_typed(const IdT* ids, const int32_t* emap, int64_t T, int K, int E,
                           int E_local, const void* hidden, int64_t row_bytes, const float* scales,
@@ -367,6 +460,10 @@ cudaError_t permute_typed(const IdT* ids, const int32_t* emap, int64_t T, int K,
       default: return launch_fused<IdT, uint8_t, kFusedV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
     }
   }
+  const OnepassPlan g = onepass_plan(T, K, E, E_local, emap != nullptr, row_bytes, d);
+  if (use_onepass(emap, vb, out, g))
+    return launch_onepass<IdT>(g, ids, emap, T, K, E, E_local, hidden, row_bytes, scales,
+                               scale_cols, out, out_scales, R, offsets, pidx, inv, hdr, s);
   cudaError_t err = launch_route<IdT>(ids, emap, T, K, E, E_local, offsets, pidx, inv, hdr, d, s);
   if (err != cudaSuccess || out == nullptr) return err;
   return launch_gather_any(vb, hidden, row_bytes, scales, scale_cols, inv, T, K,
@@ -409,6 +506,18 @@ cudaError_t permute_quant_typed(const IdT* ids, const int32_t* emap, int64_t T, 
   const int64_t row_vecs = H / 8;
   const int64_t blocks = ceil_div(row_items(T, row_vecs, kQuantV), kRowWarps);
   if (blocks > INT32_MAX) return cudaErrorInvalidConfiguration;
+  if (aligned(codes, 16)) {
+    // 16-byte code stores; float4 scale stores when every row's scales are
+    // whole 16-byte groups of four
+    if ((H / MOE_QUANT_GROUP) % 4 == 0 && aligned(scales, 16))
+      return launch(k_gather_quant_fp8_wide<true>, static_cast<unsigned>(blocks), kRowThreads, 0,
+                    s, static_cast<const uint4*>(hidden), row_vecs,
+                    static_cast<const int32_t*>(inv), T, K, static_cast<uint4*>(codes), scales,
+                    T * K);
+    return launch(k_gather_quant_fp8_wide<false>, static_cast<unsigned>(blocks), kRowThreads, 0,
+                  s, static_cast<const uint4*>(hidden), row_vecs, static_cast<const int32_t*>(inv),
+                  T, K, static_cast<uint4*>(codes), scales, T * K);
+  }
   return launch(k_gather_quant_fp8<kQuantV>, static_cast<unsigned>(blocks), kRowThreads, 0, s,
                 static_cast<const uint4*>(hidden), row_vecs, static_cast<const int32_t*>(inv), T,
                 K, static_cast<uint2*>(codes), scales, T * K);

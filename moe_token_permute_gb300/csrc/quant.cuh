@@ -76,6 +76,88 @@ __device__ __forceinline__ void quant_store_chunk(const uint4 (&v)[V], int64_t c
   }
 }
 
+// quant_store_chunk for items of 64 vectors (V = 2, four 128-column groups)
+// with 16-byte code stores: the codes are quantised in the load layout above,
+// then shuffled so that lane L holds the 16 codes of vectors c0 + 2L and
+// c0 + 2L + 1 (one uint4), and the item's four group scales are gathered into
+// lane 0 as one float4.  Per destination row that is one 512-byte warp store
+// of codes and one 16-byte store of scales, instead of two 256-byte code
+// stores and four 4-byte scale stores.  Requires 16-byte aligned code rows
+// (H a multiple of 16 bytes of codes and a 16-byte aligned base) and, for the
+// float4 scale store, a number of groups per row that is a multiple of 4 and
+// a 16-byte aligned scale base; otherwise the scales go out one per group.
+template <bool kScales16>
+__device__ __forceinline__ void quant_store_chunk_wide(const uint4 (&v)[2], int64_t c0,
+                                                       int64_t row_vecs, int p, unsigned valid,
+                                                       uint4* __restrict__ out_codes,
+                                                       float* __restrict__ out_scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t n_groups = row_vecs / (kQuantGroup / 8);
+  uint2 code[2];
+  float scale[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
+    float x[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(h2[j]);
+      x[2 * j] = f.x;
+      x[2 * j + 1] = f.y;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(x[j]));
+#pragma unroll
+    for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, d));
+    scale[i] = amax > 0.0f ? __fdiv_rn(amax, kE4m3Max) : 1.0f;
+    unsigned short* q2 = reinterpret_cast<unsigned short*>(&code[i]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = make_float2(__fdiv_rn(x[2 * j], scale[i]), __fdiv_rn(x[2 * j + 1], scale[i]));
+      q2[j] = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+    }
+  }
+  // Vectors 2L and 2L + 1 sit in slot L / 16 of lanes (2L) % 32 and (2L + 1) % 32.
+  const int src0 = (2 * lane) & 31, src1 = src0 + 1;
+  uint2 a[2], b[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    a[i].x = __shfl_sync(kFullMask, code[i].x, src0);
+    a[i].y = __shfl_sync(kFullMask, code[i].y, src0);
+    b[i].x = __shfl_sync(kFullMask, code[i].x, src1);
+    b[i].y = __shfl_sync(kFullMask, code[i].y, src1);
+  }
+  const int slot = lane >> 4;
+  const uint4 packed = slot == 0 ? make_uint4(a[0].x, a[0].y, b[0].x, b[0].y)
+                                 : make_uint4(a[1].x, a[1].y, b[1].x, b[1].y);
+  const int64_t pair = (c0 >> 1) + lane;             // this lane's uint4 in the row
+  const bool in_row = c0 + 2 * lane < row_vecs;      // whole groups: pairs never straddle
+  // The item's groups: g0 (slot 0, lanes 0-15), g0 + 1 (slot 0, lanes 16-31),
+  // g0 + 2 and g0 + 3 (slot 1).
+  const int64_t g0 = c0 / (kQuantGroup / 8);
+  const float hi0 = __shfl_sync(kFullMask, scale[0], 16);
+  const float hi1 = __shfl_sync(kFullMask, scale[1], 16);
+  const bool whole = g0 + 4 <= n_groups;
+  unsigned m = valid;
+  while (m != 0u) {
+    const int k = __ffs(m) - 1;
+    m &= m - 1u;
+    const int pk = __shfl_sync(kFullMask, p, k);
+    if (in_row) out_codes[static_cast<int64_t>(pk) * (row_vecs >> 1) + pair] = packed;
+    float* srow = out_scales + static_cast<int64_t>(pk) * n_groups + g0;
+    if (kScales16 && whole) {
+      if (lane == 0)
+        *reinterpret_cast<float4*>(srow) = make_float4(scale[0], hi0, scale[1], hi1);
+    } else if (lane == 0) {
+      const float sv[4] = {scale[0], hi0, scale[1], hi1};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (g0 + u < n_groups) srow[u] = sv[u];
+    }
+  }
+}
+
 template <int V>
 __global__ void __launch_bounds__(256)
 k_gather_quant_fp8(const uint4* __restrict__ hidden, int64_t row_vecs,
@@ -105,6 +187,36 @@ k_gather_quant_fp8(const uint4* __restrict__ hidden, int64_t row_vecs,
   if (valid == 0u) return;
 
   quant_store_chunk<V>(v, c0, row_vecs, p, valid, out_codes, out_scales);
+}
+
+// k_gather_quant_fp8 with the 16-byte stores of quant_store_chunk_wide
+// (items of 64 vectors).
+template <bool kScales16>
+__global__ void __launch_bounds__(256)
+k_gather_quant_fp8_wide(const uint4* __restrict__ hidden, int64_t row_vecs,
+                        const int32_t* __restrict__ inv_permuted_idx, int64_t T, int K,
+                        uint4* __restrict__ out_codes, float* __restrict__ out_scales,
+                        int64_t num_out_rows) {
+  constexpr int64_t kChunk = 64;
+  const int lane = threadIdx.x & 31;
+  const int64_t n_chunks = (row_vecs + kChunk - 1) / kChunk;
+  const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (item >= T * n_chunks) return;
+  const int64_t t = item / n_chunks;
+  const int64_t c0 = (item - t * n_chunks) * kChunk;
+
+  uint4 v[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int64_t c = c0 + i * 32 + lane;
+    v[i] = c < row_vecs ? ld_stream(hidden + t * row_vecs + c) : make_uint4(0, 0, 0, 0);
+  }
+  pdl_wait();
+  int p = lane < K ? __ldcg(inv_permuted_idx + t * K + lane) : -1;
+  if (p >= num_out_rows) p = -1;  // only a routing grid that gave up leaves such values
+  const unsigned valid = __ballot_sync(kFullMask, p >= 0);
+  if (valid == 0u) return;
+  quant_store_chunk_wide<kScales16>(v, c0, row_vecs, p, valid, out_codes, out_scales);
 }
 
 }  // namespace moe

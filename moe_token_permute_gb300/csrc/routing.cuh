@@ -35,7 +35,7 @@ __device__ __forceinline__ int local_expert(IdT raw, const int32_t* __restrict__
     return -1;
   }
   if (emap == nullptr) return static_cast<int>(g);
-  const int e = __ldg(emap + g);
+  const int e = emap[g];  // global memory (read-only path) or a shared-memory copy
   if (e == -1) return -1;
   if (e < 0 || e >= E_local) {
     flags |= MOE_FLAG_MAP_OUT_OF_RANGE;

@@ -94,11 +94,11 @@ def assert_bytes_equal(got: np.ndarray, ref: np.ndarray, what: str, chunk_rows: 
 def assert_rows_equal_full(inp, bufs, ref_full):
     """Every kept permuted row (p < N_valid) and scale row, bit for bit."""
     n = ref_full["n_valid"]
-    assert_bytes_equal(bytes_of(bufs["ph"][:n]), ref_full["permuted_hidden"][:n].reshape(n, -1),
+    assert_bytes_equal(bytes_of(bufs["ph"][:n]), ref_full["permuted_hidden"][:n],
                        "permuted_hidden_states")
     if bufs["ps"] is not None:
         assert_bytes_equal(bytes_of(bufs["ps"][:n]),
-                           np.ascontiguousarray(ref_full["permuted_scales"][:n]).view(np.uint8).reshape(n, -1),
+                           np.ascontiguousarray(ref_full["permuted_scales"][:n]).view(np.uint8),
                            "permuted_scales")
 
 

@@ -63,3 +63,33 @@ def test_table_wait_runs_out_and_is_flagged(debug_library, name, T):
     gpu_permute(inp, metadata_only=True, bufs=bufs)
     assert_metadata_equal(bufs, ref)
     assert mp.moe_read_status(bufs["ws"]) == 0
+
+
+@pytest.mark.parametrize("name,T", [("mixtral", 4096), ("dsv2lite", 8192)])
+def test_table_wait_runs_out_with_row_copies_in_flight(debug_library, name, T):
+    """The same forced timeout on a permute that also copies rows.  With an
+    expert map (DeepSeek-V2-Lite) the single-launch kernel serves the call:
+    its row loads are in flight into shared memory when its blocks give up,
+    and its producer warp lets them land before the block exits.  Without one
+    (Mixtral) the bulk-copy gather runs after a routing grid that gave up.
+    Either way the flag is raised, nothing hangs, and the next call on the
+    same workspace is exact."""
+    from gpu_util import assert_rows_equal_full, oracle_full
+    inp = make_inputs(name, T, seed=8, with_rows=False)
+    wl = inp["wl"]
+    bufs = alloc_outputs(T, wl.K, wl.e_local, wl.H, torch.bfloat16, E=wl.E)
+    ref = oracle_full(inp)
+    assert debug_library.moe_debug_set_table_wait(1, SHORT_WAIT_NS) == b.MOE_OK
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    gpu_permute(inp, bufs=bufs)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert mp.moe_read_status(bufs["ws"]) & b.MOE_FLAG_BARRIER_TIMEOUT
+    assert elapsed < 1.0
+    assert debug_library.moe_debug_set_table_wait(0, b.TABLE_WAIT_NS) == b.MOE_OK
+    mp.moe_clear_status(bufs["ws"])
+    gpu_permute(inp, bufs=bufs)
+    assert_metadata_equal(bufs, ref)
+    assert_rows_equal_full(inp, bufs, ref)
+    assert mp.moe_read_status(bufs["ws"]) == 0

@@ -8,7 +8,7 @@ import torch
 
 import moe_token_permute_gb300 as mp
 import oracle
-from gpu_util import alloc_outputs, assert_metadata_equal, bits16, bytes_of
+from gpu_util import alloc_outputs, assert_bytes_equal, assert_metadata_equal, bits16, bytes_of
 from test_edges_gpu import custom_inputs
 from moe_token_permute_gb300.workloads import WORKLOADS, make_inputs
 
@@ -86,25 +86,51 @@ def test_quant_permute_int64_ids_and_one_group_rows(T):
     np.testing.assert_array_equal(scales[:n].cpu().numpy(), ref["permuted_scales"][:n])
 
 
-def test_quant_permute_large_sampled():
+def test_quant_permute_large_full():
     """The DeepSeek-V3-shaped layer at 32768 tokens (inputs drawn on the
-    device): metadata in full, codes and scales on sampled rows."""
+    device): metadata, every kept row's codes and scales against the oracle
+    (1.9 GB of codes)."""
     T = 32768
     inp = make_inputs("dsv3", T, seed=0, device="cuda", with_rows=False)
     hidden = bf16_rows(T, WORKLOADS["dsv3"].H, seed=1, device="cuda")
     bufs, codes, scales = run_quant(hidden, inp)
-    ids = inp["topk_ids"].cpu().numpy()
-    ref = oracle.permute(ids, WORKLOADS["dsv3"].E)
+    ref = oracle_quant_permute(hidden, inp)
     assert_metadata_equal(bufs, ref)
-    rng = np.random.default_rng(2)
     n = ref["n_valid"]
-    ps = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, 48)]))
-    toks = ref["permuted_idx"][ps] // WORKLOADS["dsv3"].K
-    q, s = oracle.quantize_fp8(bits16(hidden[torch.from_numpy(toks).cuda()]), G)
-    got_c = bytes_of(codes[torch.from_numpy(ps).cuda()])
-    got_s = scales[torch.from_numpy(ps).cuda()].cpu().numpy()
-    np.testing.assert_array_equal(got_c, q)
-    np.testing.assert_array_equal(got_s, s)
+    assert_bytes_equal(bytes_of(codes[:n]), ref["permuted_hidden"][:n], "codes")
+    np.testing.assert_array_equal(scales[:n].cpu().numpy().view(np.uint32),
+                                  ref["permuted_scales"][:n].view(np.uint32))
+    assert mp.moe_read_status(bufs["ws"]) == 0
+
+
+@pytest.mark.parametrize("H,codes_off,scales_off", [
+    (768, 0, 0),     # 6 groups a row: scales one by one, a half item at each row's end
+    (2048, 0, 4),    # scales 4-byte aligned only: one by one
+    (2048, 8, 0),    # codes 8-byte aligned only: the 8-byte code stores
+    (1152, 8, 4),    # 9 groups, both narrow
+])
+def test_quant_permute_store_variants(H, codes_off, scales_off):
+    """The quantising gather writes 16-byte code stores and float4 scale
+    stores where the output rows allow it, and narrower ones otherwise; every
+    variant must give the oracle's codes and scales bit for bit."""
+    T = 600  # 4800 expanded rows: the routing grid and the quantising gather
+    inp = make_inputs("qwen3", T, seed=H + codes_off, with_rows=False)
+    wl = inp["wl"]
+    hidden = bf16_rows(T, H, seed=H)
+    ref = oracle_quant_permute(hidden, inp)
+    R = T * wl.K
+    bufs = alloc_outputs(T, wl.K, wl.e_local, E=wl.E)
+    cflat = torch.zeros(R * H + codes_off, dtype=torch.uint8, device="cuda")
+    sflat = torch.zeros(R * (H // G) + scales_off // 4, dtype=torch.float32, device="cuda")
+    codes = cflat[codes_off:].view(R, H)
+    scales = sflat[scales_off // 4:].view(R, H // G)
+    mp.moe_permute_quant_fp8(hidden.cuda(), inp["topk_ids"].cuda(), bufs["offsets"], bufs["pidx"],
+                             bufs["inv"], bufs["ws"], codes, scales, num_experts=wl.E)
+    assert_metadata_equal(bufs, ref)
+    n = ref["n_valid"]
+    assert_bytes_equal(bytes_of(codes[:n]), ref["permuted_hidden"][:n], "codes")
+    np.testing.assert_array_equal(scales[:n].cpu().numpy().view(np.uint32),
+                                  ref["permuted_scales"][:n].view(np.uint32))
 
 
 def test_quant_permute_rejects_bad_shapes():
