@@ -450,7 +450,9 @@ def c_abi_latency(name, T, iters=300):
     the loop), medians in us: *_c_abi_issue_us = host time per call of
     back-to-back calls; *_c_abi_sync_us = one call plus a stream synchronise,
     after an idle gap; *_c_abi_device_us = CUDA events around one call after
-    an idle gap.  Empty if the probe cannot be built or run."""
+    an idle gap; launch_floor_c_abi_* = the same for a call that enqueues one
+    tiny kernel (num_tokens = 0), the floor of any call on this machine.
+    Empty if the probe cannot be built or run."""
     from moe_token_permute_gb300 import build as cuda_build
     wl = WORKLOADS[name]
     fp8 = name == "dsv3"
@@ -464,7 +466,7 @@ def c_abi_latency(name, T, iters=300):
         print(f"c_abi_latency {name} T={T}: {exc}", file=sys.stderr)
         return {}
     return {f"{op}_c_abi_{kind}_us": r[f"{op}_{kind}_us"]
-            for op in ("permute", "unpermute") for kind in ("issue", "sync", "device")}
+            for op in ("permute", "unpermute", "launch_floor") for kind in ("issue", "sync", "device")}
 
 
 def sweep(dev, peak, flush):

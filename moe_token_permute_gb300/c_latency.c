@@ -17,6 +17,9 @@
  *              result sees end to end);
  *   device_us  CUDA-event time around one call on the stream, after the same
  *              idle gap (the GPU's own latency of the call).
+ * and, as the floor every call pays on this machine, the same three figures
+ * for moe_permute with num_tokens = 0, which enqueues one tiny kernel
+ * (launch_floor_*_us).
  */
 #define _POSIX_C_SOURCE 199309L
 #include <stdint.h>
@@ -103,6 +106,13 @@ static void do_permute(struct problem *p)
     CHECK_MOE(moe_permute(p->hidden, p->dtype, p->scales, p->scale_cols, p->ids,
                           MOE_INDEX_INT32, p->emap, p->T, p->H, p->K, p->E, p->E_local,
                           p->ph, p->ps, p->offsets, p->pidx, p->inv, p->ws, p->ws_bytes,
+                          (moe_stream_t)p->s));
+}
+
+static void do_empty_permute(struct problem *p)
+{
+    CHECK_MOE(moe_permute(NULL, p->dtype, NULL, 0, NULL, MOE_INDEX_INT32, p->emap, 0, p->H, p->K,
+                          p->E, p->E_local, NULL, NULL, p->offsets, NULL, NULL, NULL, 0,
                           (moe_stream_t)p->s));
 }
 
@@ -240,14 +250,17 @@ int main(int argc, char **argv)
     CHECK_CUDA(cudaMemcpy(p.w, wts, sizeof(float) * (size_t)R, cudaMemcpyHostToDevice));
     CHECK_CUDA(cudaDeviceSynchronize());
 
-    double pi, ps, pd, ui, us, ud;
+    double pi, ps, pd, ui, us, ud, fi, fs, fd;
     measure(&p, do_permute, iters, &pi, &ps, &pd);
     measure(&p, do_unpermute, iters, &ui, &us, &ud);
+    measure(&p, do_empty_permute, iters, &fi, &fs, &fd);
     uint32_t status = 0;
     CHECK_MOE(moe_read_status(p.ws, &status, (moe_stream_t)p.s));
     printf("{\"permute_issue_us\": %.2f, \"permute_sync_us\": %.2f, \"permute_device_us\": %.2f, "
            "\"unpermute_issue_us\": %.2f, \"unpermute_sync_us\": %.2f, "
-           "\"unpermute_device_us\": %.2f, \"status\": %u, \"iters\": %d}\n",
-           pi, ps, pd, ui, us, ud, status, iters);
+           "\"unpermute_device_us\": %.2f, \"launch_floor_issue_us\": %.2f, "
+           "\"launch_floor_sync_us\": %.2f, \"launch_floor_device_us\": %.2f, "
+           "\"status\": %u, \"iters\": %d}\n",
+           pi, ps, pd, ui, us, ud, fi, fs, fd, status, iters);
     return status == 0 ? 0 : 4;
 }
