@@ -212,7 +212,7 @@ k_permute_onepass(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   if (threadIdx.x == 0) {
     s_abort = 0;
-    s_nlist = nt;
+    s_nlist = 0;
   }
   for (int i = threadIdx.x; i < kOpRouteWarps * E_local; i += kOpThreads) cnt[i] = 0;
   for (int i = threadIdx.x; i < E_local; i += kOpThreads) {
@@ -318,27 +318,14 @@ k_permute_onepass(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
     }
     s_run[e] = run;
   }
-  {
-    // the block's tokens that keep at least one row, in token order
-    constexpr int kTokPer = (kOpRouteThreads * J + kOpRouteThreads - 1) / kOpRouteThreads;
-    int f[kTokPer], sum = 0;
-#pragma unroll
-    for (int u = 0; u < kTokPer; ++u) {
-      const int i = threadIdx.x * kTokPer + u;
-      f[u] = i < nt ? s_flag[i] : 0;
-      sum += f[u];
-    }
-    int n_list;
-    int pos = op_exclusive_sum(sum, s_warp, &n_list);
-#pragma unroll
-    for (int u = 0; u < kTokPer; ++u) {
-      const int i = threadIdx.x * kTokPer + u;
-      if (f[u]) s_list[pos++] = i;
-    }
-    if (threadIdx.x == 0) s_nlist = n_list;
-    __threadfence_block();
-    op_list_arrive();  // the producer can start on the list
-  }
+  // The block's tokens that keep at least one row, one shared-memory atomic
+  // each: the list's order is free (the producer and the consumers read the
+  // same list), and no block-wide scan stands between the ranking and the
+  // histogram row the other blocks wait for.
+  for (int i = threadIdx.x; i < nt; i += kOpRouteThreads)
+    if (s_flag[i]) s_list[atomicAdd(&s_nlist, 1)] = i;
+  op_route_sync();   // s_run and the token list are complete
+  op_list_arrive();  // the producer can start on the list
   // the block's histogram row, tagged with this call's tag
   const int e_pad = (E_local + 3) & ~3;
   const unsigned tag = call_tag(s_gen);
