@@ -281,10 +281,15 @@ class Setup:
     def unpermute(self):
         self.mp.moe_unpermute(self.rows, self.w, self.inv, self.out, workspace=self.ws)
 
-    def launches_per_permute(self):
+    def launches_per_permute(self, quant=False):
         """Kernels one moe_permute (or moe_permute_quant_fp8) call launches: one
-        up to 2048 expanded rows, else the routing grid plus the gather."""
-        return 1 if self.T * self.wl.K <= 2048 else 2
+        up to 2048 expanded rows; above that one for a permute with an expert
+        map (the single-launch expert-map kernel: these buffers are 16-byte
+        aligned and every workload's blocks fit it), else the routing grid plus
+        the gather."""
+        if self.T * self.wl.K <= 2048:
+            return 1
+        return 1 if (self.emap is not None and not quant) else 2
 
     def footprint(self):
         ts = [self.hidden, self.scales, self.ids, self.w, self.rows, self.emap, self.offsets,
@@ -653,7 +658,7 @@ def main():
             st.enable_quant(dev)
     perm_bytes = s0.qbytes if args.quant else s0.pbytes
     step_bytes = perm_bytes + s0.ubytes
-    launches_per_step = s0.launches_per_permute() + 1
+    launches_per_step = s0.launches_per_permute(args.quant) + 1
 
     def do_permute(s):
         if args.quant:
