@@ -11,6 +11,9 @@
  * GPU context stays usable.  This hook makes those waits run out on purpose,
  * without any fault, trap or endless loop: every block also waits for
  * `extra_rows` table rows past the grid that no block ever writes.
+ *
+ * A second hook checks, on the GPU, the division the fp8 quantiser uses in
+ * place of an IEEE division (see moe_debug_check_quant_division).
  */
 #ifndef MOE_PERMUTE_DEBUG_H
 #define MOE_PERMUTE_DEBUG_H
@@ -37,6 +40,23 @@ extern "C" {
  * MOE_ERR_CUDA.
  */
 MOE_API int moe_debug_set_table_wait(int extra_rows, unsigned long long wait_ns);
+
+/*
+ * moe_debug_check_quant_division: moe_permute_quant_fp8 divides each element
+ * x of a 128-column group by the group's scale s = amax / 448 with an
+ * fma-corrected reciprocal (quant.cuh, div_by_scale) when s lies in
+ * [2^-100, 2^100].  This runs, on the current device, every pair (x, amax) of
+ * finite bf16 values with |x| <= amax and amax > 0 through both that division
+ * and __fdiv_rn, and writes to the HOST array counts[4]:
+ *   counts[0]  pairs checked,
+ *   counts[1]  pairs whose e4m3 codes (satfinite, round to nearest even)
+ *              differ,
+ *   counts[2]  pairs whose fp32 quotients differ while |x / s| >= 2^-12,
+ *   counts[3]  pairs outside the scale range (IEEE division there).
+ * Synchronous (about a millisecond of GPU time).  Returns MOE_OK,
+ * MOE_ERR_INVALID_ARG (counts NULL) or MOE_ERR_CUDA.
+ */
+MOE_API int moe_debug_check_quant_division(unsigned long long *counts);
 
 #ifdef __cplusplus
 }

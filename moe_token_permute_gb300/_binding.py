@@ -70,6 +70,7 @@ MOE_NOALLOC_SCRATCH_BYTES = (1 << 20) + 256
 # Exported by the debug build only (include/moe_permute_debug.h).
 DEBUG_SIGNATURES = {
     "moe_debug_set_table_wait": (ctypes.c_int, [ctypes.c_int, ctypes.c_ulonglong]),
+    "moe_debug_check_quant_division": (ctypes.c_int, [ctypes.POINTER(ctypes.c_ulonglong)]),
 }
 MOE_DEBUG_MAX_EXTRA_ROWS = 4
 TABLE_WAIT_NS = 2_000_000_000  # the production limit of a routing-table wait

@@ -970,6 +970,56 @@ extern "C" int moe_permute_noalloc(const void* hidden_states, moe_dtype_t hidden
 }
 
 #ifdef MOE_DEBUG_HOOKS
+namespace moe {
+namespace {
+// Every pair (x, amax) of finite bf16 bit patterns, amax > 0, |x| <= amax:
+// div_by_scale against __fdiv_rn (moe_debug_check_quant_division).
+__device__ unsigned long long g_div_counts[4];
+
+__global__ void k_check_quant_division() {
+  unsigned long long checked = 0, code_diff = 0, quot_diff = 0, outside = 0;
+  const uint64_t n = 1ull << 32;
+  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<uint64_t>(gridDim.x) * blockDim.x) {
+    const uint32_t ab = static_cast<uint32_t>(i >> 16), xb = static_cast<uint32_t>(i & 0xffffu);
+    if ((ab & 0x8000u) != 0u || (ab & 0x7f80u) == 0x7f80u || (xb & 0x7f80u) == 0x7f80u) continue;
+    const float amax = __uint_as_float(ab << 16), x = __uint_as_float(xb << 16);
+    if (!(amax > 0.0f) || !(fabsf(x) <= amax)) continue;
+    ++checked;
+    const float s = __fdiv_rn(amax, kE4m3Max);
+    const float qa = __fdiv_rn(x, s);
+    float qb = qa;
+    if (scale_in_range(s)) qb = div_by_scale(x, s, __frcp_rn(s));
+    else ++outside;
+    const unsigned short ca = __nv_cvt_float2_to_fp8x2(make_float2(qa, 0.f), __NV_SATFINITE, __NV_E4M3);
+    const unsigned short cb = __nv_cvt_float2_to_fp8x2(make_float2(qb, 0.f), __NV_SATFINITE, __NV_E4M3);
+    code_diff += ca != cb;
+    quot_diff += __float_as_uint(qa) != __float_as_uint(qb) && fabsf(qa) >= 0x1p-12f;
+  }
+  atomicAdd(&g_div_counts[0], checked);
+  atomicAdd(&g_div_counts[1], code_diff);
+  atomicAdd(&g_div_counts[2], quot_diff);
+  atomicAdd(&g_div_counts[3], outside);
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_debug_check_quant_division(unsigned long long* counts) {
+  if (counts == nullptr) return MOE_ERR_INVALID_ARG;
+  const unsigned long long zero[4] = {0, 0, 0, 0};
+  if (cudaMemcpyToSymbol(moe::g_div_counts, zero, sizeof zero) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  moe::k_check_quant_division<<<1216, 256>>>();
+  if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpyFromSymbol(counts, moe::g_div_counts, sizeof zero) != cudaSuccess) {
+    cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
 extern "C" int moe_debug_set_table_wait(int extra_rows, unsigned long long wait_ns) {
   if (extra_rows < 0 || extra_rows > MOE_DEBUG_MAX_EXTRA_ROWS || wait_ns == 0)
     return MOE_ERR_INVALID_ARG;

@@ -8,7 +8,8 @@
 // the gather saves a separate pass over the activations:
 //   scale = amax(|x| over the group) / 448   (1 when the group is all zero),
 //   code  = e4m3(x / scale), round to nearest even, saturating at +-448.
-// Both divisions are IEEE-rounded fp32 divisions.
+// Both divisions are IEEE-rounded fp32 divisions (x / scale through
+// div_by_scale, which returns the same value).
 //
 // Layout: a warp owns one (token, chunk) item of 32 lanes x V vectors of 8
 // bf16 values.  Vector c of a row belongs to column group c / 16, so for each
@@ -24,6 +25,29 @@ namespace moe {
 
 constexpr int kQuantGroup = 128;  // columns per scale
 constexpr float kE4m3Max = 448.0f;
+
+// x / s rounded to nearest in fp32, for an element x of a group whose scale is
+// s = amax / 448 (so |x| <= 448 s), by the correction step of division with a
+// fused multiply-add (P. Markstein, "Computation of elementary functions on the
+// IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990; also Muller
+// et al., "Handbook of Floating-Point Arithmetic", division by iteration):
+// with y = RN(1/s), q0 = RN(x y), r = x - q0 s (exact in one fma),
+// q = RN(q0 + r y).  The sign is copied from x so that -0 stays -0 (the
+// correction would return +0).  Valid when s lies in [2^-100, 2^100]: there
+// r neither underflows nor overflows for any such x, and an exhaustive GPU
+// comparison with IEEE division over every pair of finite bf16 values
+// (x, amax), |x| <= amax, gave the same e4m3 code for all of them and the
+// same fp32 quotient wherever |q| >= 2^-12 (tests/test_quant_division_gpu.py
+// repeats it through the debug build).  scale_in_range says whether s is in
+// that range; outside it the caller divides with __fdiv_rn.
+__device__ __forceinline__ bool scale_in_range(float s) {
+  return s >= 0x1p-100f && s <= 0x1p+100f;
+}
+__device__ __forceinline__ float div_by_scale(float x, float s, float y) {
+  const float q0 = __fmul_rn(x, y);
+  const float r = __fmaf_rn(-q0, s, x);
+  return copysignf(__fmaf_rn(r, y, q0), x);
+}
 
 // Quantise one (token, chunk) item held in registers (V vectors of 8 bf16
 // values per lane; lanes 0-15 and 16-31 of vector slot i cover one 128-column
@@ -57,10 +81,20 @@ __device__ __forceinline__ void quant_store_chunk(const uint4 (&v)[V], int64_t c
     const float scale = amax > 0.0f ? __fdiv_rn(amax, kE4m3Max) : 1.0f;
     uint2 packed;
     unsigned short* q2 = reinterpret_cast<unsigned short*>(&packed);
+    if (scale_in_range(scale)) {
+      const float y = __frcp_rn(scale);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = make_float2(__fdiv_rn(x[2 * j], scale), __fdiv_rn(x[2 * j + 1], scale));
-      q2[j] = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = make_float2(div_by_scale(x[2 * j], scale, y),
+                                     div_by_scale(x[2 * j + 1], scale, y));
+        q2[j] = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = make_float2(__fdiv_rn(x[2 * j], scale), __fdiv_rn(x[2 * j + 1], scale));
+        q2[j] = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+      }
     }
     const int64_t g = c / (kQuantGroup / 8);
     unsigned m = valid;
@@ -112,10 +146,21 @@ __device__ __forceinline__ void quant_store_chunk_wide(const uint4 (&v)[2], int6
     for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, d));
     scale[i] = amax > 0.0f ? __fdiv_rn(amax, kE4m3Max) : 1.0f;
     unsigned short* q2 = reinterpret_cast<unsigned short*>(&code[i]);
+    if (scale_in_range(scale[i])) {
+      const float y = __frcp_rn(scale[i]);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f = make_float2(__fdiv_rn(x[2 * j], scale[i]), __fdiv_rn(x[2 * j + 1], scale[i]));
-      q2[j] = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = make_float2(div_by_scale(x[2 * j], scale[i], y),
+                                     div_by_scale(x[2 * j + 1], scale[i], y));
+        q2[j] = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f =
+            make_float2(__fdiv_rn(x[2 * j], scale[i]), __fdiv_rn(x[2 * j + 1], scale[i]));
+        q2[j] = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
+      }
     }
   }
   // Vectors 2L and 2L + 1 sit in slot L / 16 of lanes (2L) % 32 and (2L + 1) % 32.

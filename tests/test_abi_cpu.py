@@ -51,7 +51,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_debug_hook_only_in_debug_build(lib):
     debug_names = declared_symbols(debug=True)
-    assert debug_names == {"moe_debug_set_table_wait"}
+    assert debug_names == {"moe_debug_set_table_wait", "moe_debug_check_quant_division"}
     for n in debug_names:
         assert not hasattr(lib, n), f"{n} leaked into the production library"
     dlib = b.debug_lib()
@@ -63,6 +63,10 @@ def test_debug_hook_only_in_debug_build(lib):
 @pytest.mark.parametrize("args", [(-1, 1000), (b.MOE_DEBUG_MAX_EXTRA_ROWS + 1, 1000), (1, 0)])
 def test_debug_hook_rejects_bad_arguments_on_host(lib, args):
     assert b.debug_lib().moe_debug_set_table_wait(*args) == b.MOE_ERR_INVALID_ARG
+
+
+def test_division_check_rejects_null_on_host(lib):
+    assert b.debug_lib().moe_debug_check_quant_division(None) == b.MOE_ERR_INVALID_ARG
 
 
 def test_library_built_for_sm103a_only():
