@@ -239,15 +239,14 @@ k_permute_onepass(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
   // ---------------------------------------------------------- producer ---
   if (warp == kOpProducerWarp) {
     op_list_wait();
-    // Lane l issues items l, l + 32, ...: one thread's bulk copies go out one
-    // after another, so a single issuing thread per SM left the ring filling
-    // at a fraction of the HBM rate (measured on GB300: 54 loads of 4 KB took
-    // 18 us to issue from one thread).
-    // Lane l owns stages l, l + 32, ... and fills each with its items
-    // i = round * N + s in round order, so a stage's rounds are issued by one
-    // thread, one after another: the empty-phase wait before round r can only
-    // find the stage in phase r - 1 (not yet released) or r (released), never
-    // further behind, and its parity test cannot alias.
+    // All 32 lanes issue loads: one thread's bulk copies go out one after
+    // another, so a single issuing thread per SM left the ring filling at a
+    // fraction of the HBM rate (measured on GB300: 54 loads of 4 KB took 18 us
+    // to issue from one thread).  Lane l owns stages l, l + 32, ... and fills
+    // each with its items i = round * N + s in round order, so a stage's
+    // rounds are issued by one thread, one after another: the empty-phase wait
+    // before round r can only find the stage in phase r - 1 (not yet released)
+    // or r (released), never further behind, and its parity test cannot alias.
     const int n_items = s_nlist * n_chunks;
     bool stop = false;
     for (int round = 0; !stop; ++round) {

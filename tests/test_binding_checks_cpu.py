@@ -156,3 +156,19 @@ def test_unpermute_right_sizes_reach_the_pointers():
 def test_unpermute_refuses_small_buffers(over, what):
     with pytest.raises(ValueError, match=what):
         call_unpermute(**over)
+
+
+@pytest.mark.parametrize("dst,msg", [
+    (torch.zeros(1, dtype=torch.float32), "32-bit integer"),   # not an integer
+    (torch.zeros(1, dtype=torch.int64), "32-bit integer"),     # 8-byte elements
+    (torch.zeros(0, dtype=torch.int32), "32-bit integer"),     # no room for the word
+    (torch.zeros(4, dtype=torch.int32)[::2], "contiguous"),
+    (torch.zeros(1, dtype=torch.int32), "pinned host memory"),  # pageable host memory
+])
+def test_async_status_read_refuses_unusable_destinations(dst, msg):
+    """moe_permute_read_status writes the status word through dst from a
+    kernel: dst must be one 32-bit word of device or pinned host memory, which
+    the binding checks before taking any pointer."""
+    ws = torch.zeros(1 << 12, dtype=torch.uint8)
+    with pytest.raises(ValueError, match=msg):
+        mp.moe_permute_read_status(ws, dst)
