@@ -715,9 +715,38 @@ def main():
     torch.cuda.synchronize()
     eager_ms_per_step = max_over_ranks(start.elapsed_time(end), dist, dev) / n
 
-    # Second pass over the same K steps with events around each call: the
-    # per-op split and the duration of the dominant kernel (k_unpermute, one
-    # launch per moe_unpermute call) for the roofline.
+    # Per-op split and the duration of the dominant kernel (k_unpermute, one
+    # launch per moe_unpermute call) for the roofline: the K calls of each op
+    # captured into one CUDA graph per op (the two input sets alternate as in
+    # the steps) and replayed with one event pair around each replay, so the
+    # calls keep their back-to-back launch overlap as in the timed steps
+    # (median of 3 replays).  The split with an event pair around every eager
+    # call is kept as eager_us_per_call: each call then also pays its launch.
+    def op_graph(fn):
+        g = torch.cuda.CUDAGraph()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(n):
+                fn(sets[i % 2])
+        g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    def replay_us(g, reps=3):
+        times = []
+        for _ in range(reps):
+            start.record()
+            g.replay()
+            end.record()
+            torch.cuda.synchronize()
+            times.append(1e3 * start.elapsed_time(end) / n)
+        return statistics.median(times)
+
+    g_op = op_graph(do_permute)
+    perm_us = max_over_ranks(replay_us(g_op) / 1e3, dist, dev) * 1e3
+    g_op = op_graph(lambda st: st.unpermute())
+    unp_us = max_over_ranks(replay_us(g_op) / 1e3, dist, dev) * 1e3
+    del g_op
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
     for i in range(n):
         s = sets[i % 2]
@@ -727,8 +756,8 @@ def main():
         s.unpermute()
         ev[i][2].record()
     torch.cuda.synchronize()
-    perm_us = 1e3 * sum(e[0].elapsed_time(e[1]) for e in ev) / n
-    unp_us = 1e3 * sum(e[1].elapsed_time(e[2]) for e in ev) / n
+    perm_eager_us = 1e3 * sum(e[0].elapsed_time(e[1]) for e in ev) / n
+    unp_eager_us = 1e3 * sum(e[1].elapsed_time(e[2]) for e in ev) / n
 
     # end to end: pinned host inputs in, result out, every step
     n_e2e = min(n, 50)
@@ -767,9 +796,11 @@ def main():
             "permute": {"us_per_call": round(perm_us, 2), "GBps": round(perm_bytes / perm_us / 1e3, 1),
                         "frac": round(perm_bytes / perm_us / 1e3 / peak, 4), "bytes": perm_bytes,
                         "launches": launches_per_step - 1,
-                        "op": "moe_permute_quant_fp8" if args.quant else "moe_permute"},
+                        "op": "moe_permute_quant_fp8" if args.quant else "moe_permute",
+                        "eager_us_per_call": round(perm_eager_us, 2)},
             "unpermute": {"us_per_call": round(unp_us, 2), "GBps": round(unp_gbs, 1),
-                          "frac": round(unp_gbs / peak, 4), "bytes": s0.ubytes, "launches": 1},
+                          "frac": round(unp_gbs / peak, 4), "bytes": s0.ubytes, "launches": 1,
+                          "eager_us_per_call": round(unp_eager_us, 2)},
             "roofline": {"kernel": "k_unpermute", "bound": "hbm", "achieved": round(unp_gbs, 1),
                          "peak": peak, "unit": "GB/s", "frac": round(unp_gbs / peak, 4),
                          "peak_kind": peak_kind,
@@ -783,7 +814,9 @@ def main():
                     "serial_ms_per_step": round(e2e_serial_ms, 4),
                     "serial_value": round(job_gbs(world, step_bytes, e2e_serial_ms), 1)},
             "gpu_launches": n * launches_per_step,
-            "per_op_timing": "second pass of the same steps with CUDA events around each call",
+            "per_op_timing": "the K calls of each op replayed from one CUDA graph per op (inputs "
+                             "alternating as in the steps), events around each replay; "
+                             "eager_us_per_call: events around each eager call",
             "clocks": clk.summary(),
         }
     del e2e  # frees the pinned host copies before the sweep
