@@ -51,6 +51,11 @@ MUTANTS = {
                                         "if (inv[t * K + k] >= num_rows)"),
     "quant_zero_group_scale": ("float scale = amax > 0.0f ? amax / 448.0f : 1.0f;",
                                "float scale = amax > 0.0f ? amax / 448.0f : 0.0f;"),
+    "unpermute_k_descending": ("            for (int32_t k = 0; k < K; ++k) {\n                int32_t p = inv[t * K + k];",
+                               "            for (int32_t k = K - 1; k >= 0; --k) {\n                int32_t p = inv[t * K + k];"),
+    "unpermute_wide_accumulator": ("            float acc = 0.0f;", "            double acc = 0.0;"),
+    "unpermute_fused_multiply_add": ("                float prod = w[t * K + k] * x;\n                acc = acc + prod;",
+                                     "                acc = fmaf(w[t * K + k], x, acc);"),
 }
 
 CHILD = r"""
