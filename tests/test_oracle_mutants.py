@@ -54,6 +54,8 @@ MUTANTS = {
     "unpermute_k_descending": ("            for (int32_t k = 0; k < K; ++k) {\n                int32_t p = inv[t * K + k];",
                                "            for (int32_t k = K - 1; k >= 0; --k) {\n                int32_t p = inv[t * K + k];"),
     "unpermute_wide_accumulator": ("            float acc = 0.0f;", "            double acc = 0.0;"),
+    "quant_code_times_reciprocal": ("orc_f32_to_e4m3_satfinite(orc_bf16_to_f32(xg[i]) / scale);",
+                                    "orc_f32_to_e4m3_satfinite(orc_bf16_to_f32(xg[i]) * (1.0f / scale));"),
     "unpermute_fused_multiply_add": ("                float prod = w[t * K + k] * x;\n                acc = acc + prod;",
                                      "                acc = fmaf(w[t * K + k], x, acc);"),
 }
