@@ -187,6 +187,10 @@ unsigned item_grid(int64_t items, int warps_per_block, const DeviceInfo* d, int 
   return static_cast<unsigned>(std::max<int64_t>(1, std::min(need, cap)));
 }
 
+// From this many tokens the quantising single launch loads each warp's first
+// row chunk before the ranking (k_permute_fused, kEarly).
+constexpr int64_t kFusedEarlyMinTokens = 32;
+
 template <typename IdT, typename VecT, int V, bool kQuant = false>
 cudaError_t launch_fused(const IdT* ids, const int32_t* emap, int64_t T, int K, int E, int E_local,
                          const void* hidden, int64_t row_bytes, const float* scales,
@@ -196,7 +200,9 @@ cudaError_t launch_fused(const IdT* ids, const int32_t* emap, int64_t T, int K, 
   const int64_t R = T * K;
   const int64_t rank_warps = ceil_div(R, 32 * kMetaRowsPerLane);
   const size_t smem = (static_cast<size_t>(rank_warps) * E_local + E_local + 1 + R) * sizeof(int);
-  auto kern = k_permute_fused<IdT, VecT, V, kQuant>;
+  auto kern = k_permute_fused<IdT, VecT, V, kQuant, false>;
+  if constexpr (kQuant)
+    if (T >= kFusedEarlyMinTokens) kern = k_permute_fused<IdT, VecT, V, kQuant, true>;
   cudaError_t err = allow_smem(kern, smem);
   if (err != cudaSuccess) return err;
   const int64_t row_vecs = row_bytes / static_cast<int64_t>(sizeof(VecT));

@@ -129,7 +129,13 @@ __device__ __forceinline__ void load_item(const VecT* __restrict__ src, int64_t 
 // written as fp8 e4m3 codes (permuted_hidden reinterpreted as uint2) plus one
 // fp32 scale per 128 columns (permuted_scales), by the same arithmetic as
 // k_gather_quant_fp8.
-template <typename IdT, typename VecT, int V, bool kQuant = false>
+// kEarly: each warp loads the row chunk of its first copy item before the
+// ranking, so that load overlaps the routing.  The launch takes it only for
+// the quantising copy from kFusedEarlyMinTokens tokens: measured on GB300
+// (DeepSeek-V3 shape) 6% faster at T = 64 and 128, equal at 256, 5% slower at
+// T = 1; for the plain copy it was up to 14% slower at small T and never
+// more than 3% faster.
+template <typename IdT, typename VecT, int V, bool kQuant = false, bool kEarly = false>
 __global__ void __launch_bounds__(kMetaThreads, 1)
 k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
                 int64_t T, int K, int E, int E_local,
@@ -151,6 +157,19 @@ k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
   const bool writer = blockIdx.x == 0;
 
   pdl_wait();
+  VecT v0[V];  // kEarly: the row chunk of this warp's first copy item
+  float sc0[kPreScaleChunks];
+  if constexpr (kEarly) {
+    const int64_t nc = (row_vecs + 32 * V - 1) / (32 * V);
+    const int64_t first = blockIdx.x + static_cast<int64_t>(warp) * gridDim.x;
+    if (permuted_hidden != nullptr && first < T * nc) {
+      const int64_t t = first / nc;
+      const int64_t c0 = (first - t * nc) * (32 * V);
+      load_item<kQuant, VecT, V>(hidden + t * row_vecs, c0, row_vecs, v0);
+      if (!kQuant && permuted_scales != nullptr && c0 == 0)
+        load_token_scales(scales + t * scale_cols, scale_cols, sc0);
+    }
+  }
   for (int i = threadIdx.x; i < n_rank_warps * E_local; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
 
@@ -202,14 +221,13 @@ k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
 
   // Items go round-robin over the blocks first (item i -> block i % G), so a
   // small batch still spreads its copy over every block's SM.  A token's
-  // scales are loaded with its first row chunk, before any store.  (Loading
-  // each warp's first chunk before the ranking, to overlap the two, measured
-  // 0.2 us slower at T = 1 even when switched off at run time.)
+  // scales are loaded with its first row chunk, before any store.
   constexpr int64_t kChunk = 32 * V;
   const int64_t n_chunks = (row_vecs + kChunk - 1) / kChunk;
   const int64_t n_items = T * n_chunks;
   const int64_t G = gridDim.x;
-  for (int64_t item = blockIdx.x + warp * G; item < n_items; item += kMetaWarps * G) {
+  const int64_t item0 = blockIdx.x + warp * G;
+  for (int64_t item = item0; item < n_items; item += kMetaWarps * G) {
     const int64_t t = item / n_chunks;
     const int64_t c0 = (item - t * n_chunks) * kChunk;
     const int p = lane < K ? s_p[t * K + lane] : -1;
@@ -218,8 +236,15 @@ k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
     const bool with_scales = !kQuant && permuted_scales != nullptr && c0 == 0;
     VecT v[V];
     float sc[kPreScaleChunks];
-    load_item<kQuant, VecT, V>(hidden + t * row_vecs, c0, row_vecs, v);
-    if (with_scales) load_token_scales(scales + t * scale_cols, scale_cols, sc);
+    if (kEarly && item == item0) {  // loaded before the ranking
+#pragma unroll
+      for (int i = 0; i < V; ++i) v[i] = v0[i];
+#pragma unroll
+      for (int i = 0; i < kPreScaleChunks; ++i) sc[i] = sc0[i];
+    } else {
+      load_item<kQuant, VecT, V>(hidden + t * row_vecs, c0, row_vecs, v);
+      if (with_scales) load_token_scales(scales + t * scale_cols, scale_cols, sc);
+    }
     if constexpr (kQuant) {
       quant_store_chunk<V>(v, c0, row_vecs, p, valid, reinterpret_cast<uint2*>(permuted_hidden),
                            permuted_scales);
