@@ -282,12 +282,14 @@ class Setup:
         self.mp.moe_unpermute(self.rows, self.w, self.inv, self.out, workspace=self.ws)
 
     def launches_per_permute(self, quant=False):
-        """Kernels one moe_permute (or moe_permute_quant_fp8) call launches: one
-        up to 2048 expanded rows; above that one for a permute with an expert
-        map (the single-launch expert-map kernel: these buffers are 16-byte
-        aligned and every workload's blocks fit it), else the routing grid plus
-        the gather."""
-        if self.T * self.wl.K <= 2048:
+        """Kernels one moe_permute (or moe_permute_quant_fp8) call launches:
+        one single-launch kernel up to 2048 expanded rows for
+        moe_permute_quant_fp8, and up to 3072 (4096 with an expert map) for
+        moe_permute; above that one for a permute with an expert map (the
+        single-launch expert-map kernel: these buffers are 16-byte aligned and
+        every workload's blocks fit it), else the routing grid plus the gather."""
+        R = self.T * self.wl.K
+        if R <= (2048 if quant else 4096 if self.emap is not None else 3072):
             return 1
         return 1 if (self.emap is not None and not quant) else 2
 

@@ -3,9 +3,10 @@
  * library (compiled with -DMOE_DEBUG_HOOKS, libmoe_permute_debug.so).  The
  * production library does not export it.
  *
- * The routing grid of moe_permute (batches above 2048 expanded rows) has
- * every block read every block's row of a per-expert histogram table, waiting
- * for rows that do not carry the current call's tag yet.  Each wait is bounded
+ * The routing grid of moe_permute (batches above 3072 expanded rows without an
+ * expert map) has every block read every block's row of a per-expert
+ * histogram table, waiting for rows that do not carry the current call's tag
+ * yet.  Each wait is bounded
  * (2^24 polls or a time limit); when it runs out the block sets
  * MOE_FLAG_BARRIER_TIMEOUT in the workspace status word and returns, so the
  * GPU context stays usable.  This hook makes those waits run out on purpose,

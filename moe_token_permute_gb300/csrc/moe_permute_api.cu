@@ -7,9 +7,10 @@
 // workspace (same digest, "implementation breakdown" items 1-3).
 //
 // Dispatch:
-//   R = T*K <= kFusedMaxRows: one launch of k_permute_fused; every block
-//     redundantly ranks all rows and the blocks share the row copy (no
-//     inter-block communication);
+//   R = T*K up to 3072 rows (4096 with an expert map; 2048 for the
+//     metadata-only and the quantising permute): one launch of
+//     k_permute_fused; every block redundantly ranks all rows and the blocks
+//     share the row copy (no inter-block communication);
 //   with an expert map and 16-byte aligned rows: k_permute_onepass, one
 //     cooperative launch that routes a block of tokens and copies the rows of
 //     the tokens that keep one;
@@ -146,8 +147,25 @@ constexpr int kFusedV = 4;   // vectors per lane in one gather chunk (fused kern
 // GB300, T=1 4.0 us instead of 7.0 with 4 vectors, T=128 7.2 instead of 9.9.
 constexpr int kFusedQuantV = 1;
 constexpr int kGatherV = 8;  // same, gather kernel of the large-batch path
-constexpr int64_t kFusedMaxRows = 2048;  // R above this: routing grid + gather
+constexpr int64_t kFusedMaxRows = 2048;  // quantise-on-permute: R above this -> routing grid + gather
 static_assert(kFusedMaxRows <= kMetaChunkRows, "one block must be able to rank every row");
+// moe_permute takes the single launch a little further, ranking 4 rows per
+// lane above 2048 rows.  Measured on GB300 against the two-kernel path:
+// without a map 6-19% faster from 2200 to 3072 rows (Mixtral, Qwen3 and
+// DeepSeek-V3 shapes; DeepSeek-V3 equal at 3072) and 4-18% slower at 3584-4096;
+// with an expert map (DeepSeek-V2-Lite shape, a quarter of the rows kept)
+// 10-25% faster than the single-launch expert-map kernel up to 4096.  The
+// quantising copy measured no faster above 2048 rows and keeps kFusedMaxRows,
+// and so does the metadata-only permute, which runs as one block there (from
+// 2600 to 3072 rows 7-27% slower than the routing grid for the 128- and
+// 256-expert shapes).
+constexpr int64_t kFusedWideMaxRows = 3072;
+constexpr int64_t kFusedWideMaxRowsMap = 4096;
+static_assert(kFusedWideMaxRowsMap <= kMetaChunkRowsWide, "one block must be able to rank every row");
+
+int64_t fused_max_rows(const int32_t* emap) {
+  return emap != nullptr ? kFusedWideMaxRowsMap : kFusedWideMaxRows;
+}
 
 // (token, chunk) work items of a row kernel.
 int64_t row_items(int64_t T, int64_t row_vecs, int V) {
@@ -198,11 +216,17 @@ cudaError_t launch_fused(const IdT* ids, const int32_t* emap, int64_t T, int K, 
                          int32_t* pidx, int32_t* inv, WsHeader* hdr, const DeviceInfo* d,
                          cudaStream_t s) {
   const int64_t R = T * K;
-  const int64_t rank_warps = ceil_div(R, 32 * kMetaRowsPerLane);
+  if (R > (kQuant ? kMetaChunkRows : kMetaChunkRowsWide)) return cudaErrorInvalidConfiguration;
+  const int J = R <= kMetaChunkRows ? kMetaRowsPerLane : kMetaRowsPerLaneWide;
+  const int64_t rank_warps = ceil_div(R, 32 * J);
   const size_t smem = (static_cast<size_t>(rank_warps) * E_local + E_local + 1 + R) * sizeof(int);
   auto kern = k_permute_fused<IdT, VecT, V, kQuant, false>;
-  if constexpr (kQuant)
+  if constexpr (kQuant) {
     if (T >= kFusedEarlyMinTokens) kern = k_permute_fused<IdT, VecT, V, kQuant, true>;
+  } else {
+    if (J == kMetaRowsPerLaneWide)
+      kern = k_permute_fused<IdT, VecT, V, false, false, kMetaRowsPerLaneWide>;
+  }
   cudaError_t err = allow_smem(kern, smem);
   if (err != cudaSuccess) return err;
   const int64_t row_vecs = row_bytes / static_cast<int64_t>(sizeof(VecT));
@@ -469,7 +493,7 @@ cudaError_t permute_typed(const IdT* ids, const int32_t* emap, int64_t T, int K,
   WsHeader* hdr = static_cast<WsHeader*>(ws);
   const int64_t R = T * K;
   const size_t vb = out == nullptr ? 16 : vec_bytes(row_bytes, hidden, out);
-  if (R <= kFusedMaxRows) {
+  if (R <= (out == nullptr ? kFusedMaxRows : fused_max_rows(emap))) {
     switch (vb) {
       case 16: return launch_fused<IdT, uint4, kFusedV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);
       case 8: return launch_fused<IdT, uint2, kFusedV>(ids, emap, T, K, E, E_local, hidden, row_bytes, scales, scale_cols, out, out_scales, offsets, pidx, inv, hdr, d, s);

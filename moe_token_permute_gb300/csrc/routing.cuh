@@ -24,6 +24,10 @@ constexpr int kMetaWarps = kMetaThreads / kWarpSize;
 // from T = 1 up to R = 1024, equal at R = 2048).
 constexpr int kMetaRowsPerLane = 2;  // J
 constexpr int kMetaChunkRows = kMetaThreads * kMetaRowsPerLane;  // rows one block ranks: 2048
+// J = 4 lets one block rank up to 4096 rows: the single-launch permute serves
+// batches a little above 2048 rows with it (the dispatch says which).
+constexpr int kMetaRowsPerLaneWide = 4;
+constexpr int kMetaChunkRowsWide = kMetaThreads * kMetaRowsPerLaneWide;  // 4096
 
 // Local expert of one global id, or -1 when the row is dropped.
 template <typename IdT>

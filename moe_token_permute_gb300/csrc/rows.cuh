@@ -119,8 +119,9 @@ __device__ __forceinline__ void load_item(const VecT* __restrict__ src, int64_t 
   }
 }
 
-// Single-launch permute for small batches (at most kMetaChunkRows = 2048 expanded rows,
-// where it measured faster than the two-kernel path).  Every block
+// Single-launch permute for small batches (at most kMetaChunkRows = 2048 expanded rows
+// with J = 2 rows per lane, up to 4096 with J = 4; the dispatch takes it where
+// it measured faster than the two-kernel path).  Every block
 // computes the whole stable counting sort in shared memory (R is small, the
 // ids come from L2), block 0 writes the metadata, and all blocks share the
 // row copy: no block ever waits for another.
@@ -135,7 +136,8 @@ __device__ __forceinline__ void load_item(const VecT* __restrict__ src, int64_t 
 // (DeepSeek-V3 shape) 6% faster at T = 64 and 128, equal at 256, 5% slower at
 // T = 1; for the plain copy it was up to 14% slower at small T and never
 // more than 3% faster.
-template <typename IdT, typename VecT, int V, bool kQuant = false, bool kEarly = false>
+template <typename IdT, typename VecT, int V, bool kQuant = false, bool kEarly = false,
+          int J = kMetaRowsPerLane>
 __global__ void __launch_bounds__(kMetaThreads, 1)
 k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
                 int64_t T, int K, int E, int E_local,
@@ -147,8 +149,8 @@ k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
   extern __shared__ int smem[];
   __shared__ int s_warp[32];
   const int64_t R = T * K;
-  // warps that own at least one row (each owns 32 * kMetaRowsPerLane rows)
-  const int n_rank_warps = static_cast<int>((R + 32 * kMetaRowsPerLane - 1) / (32 * kMetaRowsPerLane));
+  // warps that own at least one row (each owns 32 * J rows)
+  const int n_rank_warps = static_cast<int>((R + 32 * J - 1) / (32 * J));
   int* cnt = smem;
   int* s_base = cnt + n_rank_warps * E_local;
   int* s_p = s_base + E_local + 1;
@@ -173,12 +175,12 @@ k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
   for (int i = threadIdx.x; i < n_rank_warps * E_local; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
 
-  const int64_t slice0 = static_cast<int64_t>(warp) * 32 * kMetaRowsPerLane;
-  int key[kMetaRowsPerLane], rank[kMetaRowsPerLane];
+  const int64_t slice0 = static_cast<int64_t>(warp) * 32 * J;
+  int key[J], rank[J];
   if (warp < n_rank_warps) {
     unsigned flags = 0;
-    load_keys<IdT, kMetaRowsPerLane>(ids, emap, E, E_local, slice0, R, key, flags);
-    rank_warp_slice<kMetaRowsPerLane>(key, cnt + warp * E_local, rank);
+    load_keys<IdT, J>(ids, emap, E, E_local, slice0, R, key, flags);
+    rank_warp_slice<J>(key, cnt + warp * E_local, rank);
     if (writer) {
       flags = __reduce_or_sync(kFullMask, flags);
       if (flags != 0 && lane == 0) atomicOr(&hdr->status, flags);
@@ -201,7 +203,7 @@ k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
 
   if (warp < n_rank_warps) {
 #pragma unroll
-    for (int j = 0; j < kMetaRowsPerLane; ++j) {
+    for (int j = 0; j < J; ++j) {
       const int64_t r = slice0 + j * 32 + lane;
       if (r < R) {
         const int e = key[j];

@@ -75,10 +75,23 @@ def test_zero_tokens():
 
 
 @pytest.mark.parametrize("T,K", [(2048, 1), (2049, 1), (256, 8), (257, 8),
+                                 (3072, 1), (3073, 1), (384, 8), (385, 8),
                                  (CHUNK, 1), (CHUNK + 1, 1), (1024, 8), (1025, 8),
                                  (3 * CHUNK // 2 + 3, 2), (5 * CHUNK + 17, 1)])
 def test_single_and_multi_launch_boundary(T, K):
+    """Around 2048 rows (one block ranks 2 rows per lane, then 4), 3072 (the
+    single launch ends without a map) and the routing grid's round sizes."""
     check_case(custom_inputs(T, K, 64, 96, seed=T))
+
+
+@pytest.mark.parametrize("T,K", [(2048, 2), (2049, 2), (4096, 1), (4097, 1), (512, 8), (513, 8)])
+def test_single_launch_boundary_with_expert_map(T, K):
+    """With an expert map the single launch serves up to 4096 rows, and the
+    single-launch expert-map kernel takes over above."""
+    g = torch.Generator().manual_seed(T + K)
+    emap = torch.full((64,), -1, dtype=torch.int32)
+    emap[torch.randperm(64, generator=g)[:16]] = torch.randperm(16, generator=g).to(torch.int32)
+    check_case(custom_inputs(T, K, 64, 128, E_local=16, emap=emap, seed=T + K))
 
 
 @pytest.mark.parametrize("H,dtype", [(1, torch.bfloat16), (3, torch.bfloat16),
@@ -122,15 +135,18 @@ def test_max_topk_and_max_local_experts(T):
     check_case(custom_inputs(T, K, E, 64, seed=5))
 
 
-@pytest.mark.parametrize("T,K", [(256, 8), (2048, 1), (1, 32)])
+@pytest.mark.parametrize("T,K", [(256, 8), (2048, 1), (1, 32), (384, 8)])
 def test_single_launch_with_max_local_experts(T, K):
-    """Up to 2048 rows over 1024 experts in one launch: every warp ranks, and
-    the per-warp counts take [32][1024] ints of shared memory."""
+    """Up to 3072 rows over 1024 experts in one launch: every warp ranks (2 or
+    4 rows per lane), and the per-warp counts take up to [32][1024] ints of
+    shared memory."""
     check_case(custom_inputs(T, K, mp.MOE_MAX_LOCAL_EXPERTS, 64, seed=T + K))
 
 
-@pytest.mark.parametrize("T", [700, 9000])
+@pytest.mark.parametrize("T", [682, 700, 9000])
 def test_expert_map_with_max_local_experts(T):
+    """1024 local experts of 2048 through an expert map: one launch of the
+    small-batch kernel at 4092 rows, the expert-map kernel above."""
     E, EL = 2048, 1024
     g = torch.Generator().manual_seed(3)
     emap = torch.full((E,), -1, dtype=torch.int32)

@@ -1,4 +1,4 @@
-"""Permute with an expert map above 2048 expanded rows, against the oracle.
+"""Permute with an expert map above 4096 expanded rows, against the oracle.
 
 With an expert map and 16-byte aligned rows, moe_permute routes each block of
 tokens and copies the rows of the tokens that keep one in a single launch.
@@ -40,7 +40,7 @@ CASES = {
     "top8_4_rows_per_lane": (30000, 8, 128, 32, 256, torch.bfloat16, 0),
     "wide_rows_ragged_chunks": (3000, 2, 16, 5, 5000, torch.bfloat16, 0),
     "fp8_rows_with_scales": (2000, 8, 256, 64, 7168, torch.float8_e4m3fn, 56),
-    "1024_local_experts": (1000, 4, 2048, 1024, 64, torch.bfloat16, 0),
+    "1024_local_experts": (1100, 4, 2048, 1024, 64, torch.bfloat16, 0),
     "one_local_expert": (5000, 2, 64, 1, 128, torch.bfloat16, 0),
     "many_refill_rounds": (20000, 1, 2048, 1024, 4096, torch.bfloat16, 0),
     "fp32_rows": (3000, 3, 40, 10, 24, torch.float32, 0),

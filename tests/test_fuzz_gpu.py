@@ -32,8 +32,8 @@ MAX_ELEMS = 6_000_000  # cap on T*K*H (the unpermute input), so the oracle finis
 def draw(seed):
     rng = np.random.default_rng(7919 + seed)
     K = int(rng.choice([1, 2, 3, 4, 6, 8, 8, 13, 32], p=[.1, .2, .1, .15, .1, .15, .05, .05, .1]))
-    if rng.random() < 0.4:  # around the single-launch limit R = T*K <= 2048
-        T = max(1, 2048 // K + int(rng.integers(-2, 3)))
+    if rng.random() < 0.4:  # around the single launch's limits: 2048 rows (2 -> 4 rows per lane), 3072 (its end without a map)
+        T = max(1, int(rng.choice([2048, 3072])) // K + int(rng.integers(-2, 3)))
     else:
         T = int(np.exp(rng.uniform(0, np.log(7000))))
     E = int(rng.integers(1, 300))

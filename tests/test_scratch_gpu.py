@@ -8,7 +8,7 @@ batch and then the smaller one, as a serving loop would.  Each call is compared
 element by element with the oracle (offsets, both index maps, every kept row
 and fp8 scale row, the unpermuted tokens), and every returned tensor must be a
 view of the storage allocated at construction.  The two batch sizes straddle
-the single-launch / routing-grid boundary (2048 expanded rows).
+the boundary between the single-launch kernel and the larger-batch paths.
 """
 import numpy as np
 import pytest
