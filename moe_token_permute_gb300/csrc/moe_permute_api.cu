@@ -151,7 +151,7 @@ constexpr int64_t kFusedMaxRows = 2048;  // quantise-on-permute: R above this ->
 static_assert(kFusedMaxRows <= kMetaChunkRows, "one block must be able to rank every row");
 // moe_permute takes the single launch a little further, ranking 4 rows per
 // lane above 2048 rows.  Measured on GB300 against the two-kernel path:
-// without a map 6-19% faster from 2200 to 3072 rows (Mixtral, Qwen3 and
+// without a map 7-24% faster from 2080 to 3072 rows (Mixtral, Qwen3 and
 // DeepSeek-V3 shapes; DeepSeek-V3 equal at 3072) and 4-18% slower at 3584-4096;
 // with an expert map (DeepSeek-V2-Lite shape, a quarter of the rows kept)
 // 10-25% faster than the single-launch expert-map kernel up to 4096.  The

@@ -133,8 +133,8 @@ __device__ __forceinline__ void load_item(const VecT* __restrict__ src, int64_t 
 // kEarly: each warp loads the row chunk of its first copy item before the
 // ranking, so that load overlaps the routing.  The launch takes it only for
 // the quantising copy from kFusedEarlyMinTokens tokens: measured on GB300
-// (DeepSeek-V3 shape) 6% faster at T = 64 and 128, equal at 256, 5% slower at
-// T = 1; for the plain copy it was up to 14% slower at small T and never
+// (DeepSeek-V3 shape) 5-10% faster at T = 32 to 128, equal at 256, 5% slower
+// at T = 1; for the plain copy it was up to 14% slower at small T and never
 // more than 3% faster.
 template <typename IdT, typename VecT, int V, bool kQuant = false, bool kEarly = false,
           int J = kMetaRowsPerLane>
