@@ -51,20 +51,15 @@ __device__ __forceinline__ float div_by_scale(float x, float s, float y) {
 
 // Quantise one (token, chunk) item held in registers (V vectors of 8 bf16
 // values per lane; lanes 0-15 and 16-31 of vector slot i cover one 128-column
-// group each) and store codes and scales to every destination row p_k whose
-// bit k is set in `valid` (lane k < K holds p_k in `p`).  Every lane of the
-// warp must call it (the group maxima are half-warp shuffles); vectors at or
-// beyond row_vecs are not stored.
+// group each): codes[i] holds the lane's 8 e4m3 codes of vector i, scales[i]
+// its group's scale.  Every lane of the warp must call it (the group maxima
+// are half-warp shuffles).  It needs no destination, so the kernels run it
+// before they wait for the routing positions.
 template <int V>
-__device__ __forceinline__ void quant_store_chunk(const uint4 (&v)[V], int64_t c0,
-                                                  int64_t row_vecs, int p, unsigned valid,
-                                                  uint2* __restrict__ out_codes,
-                                                  float* __restrict__ out_scales) {
-  const int lane = threadIdx.x & 31;
-  const int64_t n_groups = row_vecs / (kQuantGroup / 8);
+__device__ __forceinline__ void quant_chunk(const uint4 (&v)[V], uint2 (&codes)[V],
+                                            float (&scales)[V]) {
 #pragma unroll
   for (int i = 0; i < V; ++i) {
-    const int64_t c = c0 + i * 32 + lane;
     const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&v[i]);
     float x[8];
 #pragma unroll
@@ -79,8 +74,7 @@ __device__ __forceinline__ void quant_store_chunk(const uint4 (&v)[V], int64_t c
 #pragma unroll
     for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, d));
     const float scale = amax > 0.0f ? __fdiv_rn(amax, kE4m3Max) : 1.0f;
-    uint2 packed;
-    unsigned short* q2 = reinterpret_cast<unsigned short*>(&packed);
+    unsigned short* q2 = reinterpret_cast<unsigned short*>(&codes[i]);
     if (scale_in_range(scale)) {
       const float y = __frcp_rn(scale);
 #pragma unroll
@@ -96,6 +90,24 @@ __device__ __forceinline__ void quant_store_chunk(const uint4 (&v)[V], int64_t c
         q2[j] = __nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3);
       }
     }
+    scales[i] = scale;
+  }
+}
+
+// Store an item quantised by quant_chunk to every destination row p_k whose
+// bit k is set in `valid` (lane k < K holds p_k in `p`): 8 bytes of codes per
+// lane and one scale per half-warp.  Vectors at or beyond row_vecs are not
+// stored.
+template <int V>
+__device__ __forceinline__ void store_quant_chunk(const uint2 (&codes)[V], const float (&scales)[V],
+                                                  int64_t c0, int64_t row_vecs, int p,
+                                                  unsigned valid, uint2* __restrict__ out_codes,
+                                                  float* __restrict__ out_scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t n_groups = row_vecs / (kQuantGroup / 8);
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int64_t c = c0 + i * 32 + lane;
     const int64_t g = c / (kQuantGroup / 8);
     unsigned m = valid;
     while (m != 0u) {
@@ -103,14 +115,14 @@ __device__ __forceinline__ void quant_store_chunk(const uint4 (&v)[V], int64_t c
       m &= m - 1u;
       const int pk = __shfl_sync(kFullMask, p, k);
       if (c < row_vecs) {
-        out_codes[static_cast<int64_t>(pk) * row_vecs + c] = packed;
-        if ((lane & 15) == 0) out_scales[static_cast<int64_t>(pk) * n_groups + g] = scale;
+        out_codes[static_cast<int64_t>(pk) * row_vecs + c] = codes[i];
+        if ((lane & 15) == 0) out_scales[static_cast<int64_t>(pk) * n_groups + g] = scales[i];
       }
     }
   }
 }
 
-// quant_store_chunk for items of 64 vectors (V = 2, four 128-column groups)
+// quant_chunk / store_quant_chunk for items of 64 vectors (V = 2, four 128-column groups)
 // with 16-byte code stores, in two steps: quant_chunk_wide quantises (it needs
 // no destination, so the gather runs it before it waits for the routing grid:
 // measured on GB300, DeepSeek-V3 quantise-on-permute 1-5% faster from T = 512
@@ -242,13 +254,15 @@ k_gather_quant_fp8(const uint4* __restrict__ hidden, int64_t row_vecs,
   }
   // The rows are the caller's input (complete: the routing grid has passed its
   // own dependency wait); the positions come from the routing grid.
+  uint2 codes[V];
+  float qs[V];
+  quant_chunk<V>(v, codes, qs);  // before the wait: it needs no position
   pdl_wait();
   int p = lane < K ? __ldcg(inv_permuted_idx + t * K + lane) : -1;
   if (p >= num_out_rows) p = -1;  // only a routing grid that gave up leaves such values
   const unsigned valid = __ballot_sync(kFullMask, p >= 0);
   if (valid == 0u) return;
-
-  quant_store_chunk<V>(v, c0, row_vecs, p, valid, out_codes, out_scales);
+  store_quant_chunk<V>(codes, qs, c0, row_vecs, p, valid, out_codes, out_scales);
 }
 
 // k_gather_quant_fp8 with the 16-byte stores of quant_chunk_wide /

@@ -248,8 +248,14 @@ k_permute_fused(const IdT* __restrict__ ids, const int32_t* __restrict__ emap,
       if (with_scales) load_token_scales(scales + t * scale_cols, scale_cols, sc);
     }
     if constexpr (kQuant) {
-      quant_store_chunk<V>(v, c0, row_vecs, p, valid, reinterpret_cast<uint2*>(permuted_hidden),
-                           permuted_scales);
+      // (quantising the early chunk before the ranking as well measured 6-8%
+      // slower at T = 32-256: the ranking warps carry the quantiser's
+      // registers and latency)
+      uint2 codes[V];
+      float qs[V];
+      quant_chunk<V>(v, codes, qs);
+      store_quant_chunk<V>(codes, qs, c0, row_vecs, p, valid,
+                           reinterpret_cast<uint2*>(permuted_hidden), permuted_scales);
     } else {
       store_chunk<VecT, V>(v, permuted_hidden, c0, row_vecs, p, valid);
       if (with_scales)
